@@ -1,0 +1,356 @@
+/*
+ * moe_oracle.c -- plain, slow CPU oracle of the capacity-limited top-k
+ * mixture-of-experts layer forward.  TEST INFRASTRUCTURE ONLY: it is used by
+ * the tests, by the package's smoke check and by the benchmark's CPU-baseline
+ * leg.  The CUDA library never links, calls or includes anything here, and
+ * this file shares no code, header or table with it.
+ *
+ * Every function follows one step of the method as the expert-parallelism
+ * pages state it, written out by direct loops:
+ *
+ *   [NG] "Expert Parallelism" notes page (narrativegoldmine.com):
+ *        "Components and Architecture" and
+ *        "Formal Algorithm: Expert Parallelism Forward Pass".
+ *   [TI] "Expert Parallelism" (theinfinity.ai, Systems / Distributed):
+ *        the per-device capacity and overflow paragraph and the
+ *        6-token / 8-expert / 4-device worked-example caption.
+ *   [AS] "Expert Parallelism and the All-to-All Bottleneck"
+ *        (ashishsrivastav.com): "The Mechanism of Expert Parallelism",
+ *        phases 1-4, and "The All-to-All Communication Pattern".
+ *
+ * Where the pages are silent the plainest reading is taken; each reading is
+ * named at the function that applies it.
+ *
+ * Precision: router logits in fp32 in one fixed order (the integer top-k
+ * decision is taken in the precision of the CUDA path, fp32); everything
+ * else (softmax, expert FFN, combine) in fp64.  Build with
+ * -ffp-contract=off so that only the explicit fmaf() calls are fused.
+ *
+ * Parity status per function (what pins it, see the oracle tests):
+ *   oracle_capacity        pinned (closed forms of [TI] and the workloads)
+ *   oracle_router_logits   pinned (exact small-integer dot products, fp64
+ *                          bound, tie cases)
+ *   oracle_softmax_topk    pinned (worked-example closed form, brute force)
+ *   oracle_assign          pinned ([TI] worked example, invariants, brute force)
+ *   oracle_dispatch        pinned (inverse permutation property)
+ *   oracle_expert_ffn      pinned (dense soft-MoE / plain MLP special cases
+ *                          against a library matmul)
+ *   oracle_combine         pinned (dense all-experts brute force)
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F32 0
+#define ORACLE_BF16 1
+#define ORACLE_SWIGLU 0
+#define ORACLE_GELU 1
+
+/* A bf16 value is the upper 16 bits of the fp32 with the same value. */
+static float bf16_bits_to_float(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Element i of a tensor stored as fp32 or bf16, returned exactly as fp32. */
+static float elem(const void* p, int dtype, size_t i) {
+    if (dtype == ORACLE_BF16) return bf16_bits_to_float(((const uint16_t*)p)[i]);
+    return ((const float*)p)[i];
+}
+
+/* ------------------------------------------------------------------------ *
+ * Capacity.  [TI] capacity paragraph: a device expecting B*k/D tokens
+ * provisions C = ceil((B*k/D)*c).  Per expert, as the layer drops per expert,
+ * the same rule with E in place of D: C = ceil((T*k/E)*c), evaluated in double
+ * in that order.  [NG] "Capacity Factor and Token Dropping": c times the mean
+ * load.  An expert can receive at most T assignments (the k choices of a token
+ * are distinct), so C is clamped to T; c = +inf means C = T (nothing dropped).
+ * C_shard (the per-device figure of [TI]) is clamped to T*k.
+ * rows_max = min(E*C, T*k) bounds the kept assignments.
+ * ------------------------------------------------------------------------ */
+int oracle_capacity(int64_t T, int k, int E, int D, double c,
+                    int64_t* C_expert, int64_t* C_shard, int64_t* rows_max) {
+    if (T < 0 || k < 1 || E < 1 || D < 1 || !(c > 0.0)) return 1;
+    int64_t Tk = T * (int64_t)k;
+    int64_t ce, cs;
+    if (isinf(c)) {
+        ce = T;
+        cs = Tk;
+    } else {
+        double ve = ceil(((double)Tk / (double)E) * c);
+        double vs = ceil(((double)Tk / (double)D) * c);
+        ce = ve >= (double)T ? T : (int64_t)ve;
+        cs = vs >= (double)Tk ? Tk : (int64_t)vs;
+    }
+    int64_t rm = (int64_t)E * ce;
+    if (rm > Tk) rm = Tk;
+    *C_expert = ce;
+    *C_shard = cs;
+    *rows_max = rm;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ *
+ * Router logits.  [NG] formal algorithm, gate computation: g_t = the routing
+ * linear projection of x_t, one logit per expert.  [NG] "Components and
+ * Architecture", gating network: an optional per-expert bias on the logits.
+ *
+ * Fixed summation order (the pages give none; the top-k decision must be
+ * reproducible bit for bit): one fp32 fused multiply-add chain over the
+ * hidden index in ascending order, starting from +0:
+ *     s = 0; for i = 0..d-1: s = fmaf(x[t,i], Wg[e,i], s);   g = s + b[e]
+ * Wg is [E, d] (nn.Linear out x in).
+ * ------------------------------------------------------------------------ */
+void oracle_router_logits(int64_t T, int d, int E, int dtype,
+                          const void* x, const void* Wg, const float* bias,
+                          float* logits /* [T, E] */) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            float s = 0.0f;
+            for (int i = 0; i < d; ++i)
+                s = fmaf(elem(x, dtype, (size_t)t * d + i),
+                         elem(Wg, dtype, (size_t)e * d + i), s);
+            if (bias) s = s + bias[e];
+            logits[(size_t)t * E + e] = s;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ *
+ * Softmax, top-k, gates.  [NG] formal algorithm: p_t = softmax(g_t / tau)
+ * (tau = 1, the pages fix no value); expert selection e(t) = argmax p_t with
+ * gate w_t = p_{t,e(t)}; [NG] "Components and Architecture" and the [AS]
+ * routing phase: the top-k experts are selected.
+ *
+ * Readings: softmax is strictly increasing, so the k largest p are the k
+ * largest g; ranking is done on the fp32 logits, largest first, equal logits
+ * ranked by the lower expert index.  Rank r = 0 is the largest.  The gate of
+ * choice r is the softmax probability of that expert, not renormalised over
+ * the k choices.  Softmax in double with the maximum subtracted, rounded to
+ * fp32 once.
+ * ------------------------------------------------------------------------ */
+void oracle_softmax_topk(int64_t T, int E, int k, const float* logits,
+                         float* probs /* [T, E] or NULL */,
+                         int32_t* topk_idx /* [T, k] */,
+                         float* topk_gate /* [T, k] */) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const float* g = logits + (size_t)t * E;
+        double m = g[0];
+        for (int e = 1; e < E; ++e)
+            if (g[e] > m) m = g[e];
+        double sum = 0.0;
+        for (int e = 0; e < E; ++e) sum += exp((double)g[e] - m);
+        /* chosen[] marks experts already taken by a higher rank */
+        unsigned char chosen[1024];
+        for (int e = 0; e < E; ++e) chosen[e] = 0;
+        for (int r = 0; r < k; ++r) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (chosen[e]) continue;
+                if (best < 0 || g[e] > g[best]) best = e; /* strict: ties keep lower e */
+            }
+            chosen[best] = 1;
+            topk_idx[(size_t)t * k + r] = best;
+            topk_gate[(size_t)t * k + r] = (float)(exp((double)g[best] - m) / sum);
+        }
+        if (probs)
+            for (int e = 0; e < E; ++e)
+                probs[(size_t)t * E + e] = (float)(exp((double)g[e] - m) / sum);
+    }
+}
+
+/* ------------------------------------------------------------------------ *
+ * Slot assignment and token dropping.  [NG] "Capacity Factor and Token
+ * Dropping": an expert takes at most C assignments, the rest are dropped.
+ * [TI] capacity paragraph: per-device overflow max(0, p*B*k - C), where p*B*k
+ * is the number of assignments the device receives.
+ *
+ * Reading (the pages fix no order): assignments are served in the priority
+ * (choice rank r, then token index t): every rank-0 choice in token order,
+ * then every rank-1 choice, and so on.  pos(t, r) is the number of earlier
+ * assignments in that order to the same expert; kept iff pos < C.
+ * Experts sit on shards in contiguous blocks of E/D ([AS] all-to-all pattern:
+ * 64 experts on 8 GPUs, expert 55 on GPU 6, expert 5 on GPU 0).
+ *
+ * Outputs: slot_pos (pos or -1 when dropped), per-expert routed and kept
+ * counts, expert_offsets (exclusive scan of kept counts, E+1 entries),
+ * shard_offsets[s] = expert_offsets[s*E/D] (D+1 entries), per-shard routed
+ * count and overflow, row_token[expert_offsets[e] + pos] = t for every kept
+ * (t, r), and the total number of dropped assignments.
+ * ------------------------------------------------------------------------ */
+void oracle_assign(int64_t T, int E, int D, int k, int64_t C, int64_t C_shard,
+                   const int32_t* topk_idx, int32_t* slot_pos,
+                   int32_t* counts_routed, int32_t* counts_kept,
+                   int32_t* expert_offsets, int32_t* shard_offsets,
+                   int32_t* shard_routed, int32_t* shard_overflow,
+                   int32_t* row_token, int64_t* dropped) {
+    int64_t* cnt = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t ndrop = 0;
+    for (int r = 0; r < k; ++r) {
+        for (int64_t t = 0; t < T; ++t) {
+            int e = topk_idx[(size_t)t * k + r];
+            int64_t pos = cnt[e]++;
+            if (pos < C) {
+                slot_pos[(size_t)t * k + r] = (int32_t)pos;
+            } else {
+                slot_pos[(size_t)t * k + r] = -1;
+                ++ndrop;
+            }
+        }
+    }
+    int64_t off = 0;
+    for (int e = 0; e < E; ++e) {
+        counts_routed[e] = (int32_t)cnt[e];
+        counts_kept[e] = (int32_t)(cnt[e] < C ? cnt[e] : C);
+        expert_offsets[e] = (int32_t)off;
+        off += counts_kept[e];
+    }
+    expert_offsets[E] = (int32_t)off;
+    int per = E / D;
+    for (int s = 0; s < D; ++s) {
+        int64_t routed = 0;
+        for (int e = s * per; e < (s + 1) * per; ++e) routed += cnt[e];
+        shard_routed[s] = (int32_t)routed;
+        shard_overflow[s] = (int32_t)(routed > C_shard ? routed - C_shard : 0);
+        shard_offsets[s] = expert_offsets[s * per];
+    }
+    shard_offsets[D] = expert_offsets[E];
+    for (int64_t t = 0; t < T; ++t)
+        for (int r = 0; r < k; ++r) {
+            int32_t pos = slot_pos[(size_t)t * k + r];
+            if (pos >= 0) row_token[expert_offsets[topk_idx[(size_t)t * k + r]] + pos] = (int32_t)t;
+        }
+    *dropped = ndrop;
+    free(cnt);
+}
+
+/* ------------------------------------------------------------------------ *
+ * Dispatch (pack).  [AS] phase 2: rows are repacked so that each row holds a
+ * token destined for one expert; [NG] dispatch tensor.  Here the pack is a
+ * local permutation: xd[row] = x[row_token[row]] for the kept rows, in
+ * expert-major order (and so grouped by shard).  A byte copy.
+ * ------------------------------------------------------------------------ */
+void oracle_dispatch(int64_t rows, int d, int elem_bytes, const void* x,
+                     const int32_t* row_token, void* xd) {
+    size_t rb = (size_t)d * (size_t)elem_bytes;
+    for (int64_t row = 0; row < rows; ++row)
+        memcpy((char*)xd + (size_t)row * rb, (const char*)x + (size_t)row_token[row] * rb, rb);
+}
+
+/* ------------------------------------------------------------------------ *
+ * Expert FFN of one row.  [NG] "Components and Architecture", expert GEMM: a
+ * standard transformer MLP per expert; [AS] phase 3.  Forms (no biases,
+ * weights nn.Linear out x in):
+ *   SwiGLU: a = W1[e] x, u = W3[e] x, h = a * sigmoid(a) * u, y = W2[e] h
+ *   GeLU:   a = W1[e] x, h = 0.5 a (1 + erf(a / sqrt 2)),     y = W2[e] h
+ * All in double from the stored (fp32 or bf16) values; h is not rounded.
+ * ------------------------------------------------------------------------ */
+static void ffn_row(int d, int f, int act, int dtype, const void* xrow_base, size_t xrow_off,
+                    int e, const void* W1, const void* W3, const void* W2,
+                    double* h /* scratch [f] */, double* y /* [d] */) {
+    for (int j = 0; j < f; ++j) {
+        double a = 0.0, u = 0.0;
+        for (int i = 0; i < d; ++i) {
+            double xi = elem(xrow_base, dtype, xrow_off + i);
+            a += xi * (double)elem(W1, dtype, ((size_t)e * f + j) * d + i);
+            if (act == ORACLE_SWIGLU)
+                u += xi * (double)elem(W3, dtype, ((size_t)e * f + j) * d + i);
+        }
+        if (act == ORACLE_SWIGLU)
+            h[j] = a / (1.0 + exp(-a)) * u;
+        else
+            h[j] = 0.5 * a * (1.0 + erf(a / sqrt(2.0)));
+    }
+    for (int o = 0; o < d; ++o) {
+        double s = 0.0;
+        for (int j = 0; j < f; ++j) s += h[j] * (double)elem(W2, dtype, ((size_t)e * d + o) * f + j);
+        y[o] = s;
+    }
+}
+
+/* Expert FFN over the packed rows: yd[row] = FFN_e(xd[row]) for every row of
+ * expert e, i.e. rows expert_offsets[e] .. expert_offsets[e+1]-1. */
+void oracle_expert_ffn(int E, int d, int f, int act, int dtype, const void* xd,
+                       const int32_t* expert_offsets, const void* W1, const void* W3,
+                       const void* W2, double* yd /* [rows, d] */) {
+    for (int e = 0; e < E; ++e) {
+        int64_t r0 = expert_offsets[e], r1 = expert_offsets[e + 1];
+#pragma omp parallel
+        {
+            double* h = (double*)malloc(sizeof(double) * (size_t)f);
+#pragma omp for schedule(static)
+            for (int64_t row = r0; row < r1; ++row)
+                ffn_row(d, f, act, dtype, xd, (size_t)row * d, e, W1, W3, W2, h, yd + (size_t)row * d);
+            free(h);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ *
+ * Combine.  [NG] expert combine and formal algorithm: each returned
+ * activation is multiplied by its gating weight and a token's k outputs are
+ * summed, back in token order ([AS] phase 4); then the residual ([NG]
+ * residual addition).  A dropped assignment adds nothing: the token passes
+ * through the residual only ([NG] "Capacity Factor and Token Dropping").
+ *     y[t] = residual[t] + sum over kept r of gate[t,r] * yd[row(t,r)]
+ * residual NULL means no residual term.
+ * ------------------------------------------------------------------------ */
+void oracle_combine(int64_t T, int d, int k, int dtype, const int32_t* topk_idx,
+                    const int32_t* slot_pos, const float* topk_gate,
+                    const int32_t* expert_offsets, const double* yd,
+                    const void* residual, double* y /* [T, d] */) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int o = 0; o < d; ++o) {
+            double s = 0.0;
+            for (int r = 0; r < k; ++r) {
+                int32_t pos = slot_pos[(size_t)t * k + r];
+                if (pos < 0) continue;
+                int64_t row = (int64_t)expert_offsets[topk_idx[(size_t)t * k + r]] + pos;
+                s += (double)topk_gate[(size_t)t * k + r] * yd[(size_t)row * d + o];
+            }
+            if (residual) s += (double)elem(residual, dtype, (size_t)t * d + o);
+            y[(size_t)t * d + o] = s;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ *
+ * Layer output of selected tokens, straight from the definition: for each
+ * listed token t, y[t] = residual[t] + sum over kept r of
+ * gate[t,r] * FFN_{idx[t,r]}(x[t]).  Uses x directly (not the packed rows),
+ * so the whole-layer check does not lean on dispatch.  For workloads whose
+ * full FFN is too slow on the CPU.
+ * ------------------------------------------------------------------------ */
+void oracle_token_outputs(int64_t n, const int64_t* tokens, int d, int f, int k, int act,
+                          int dtype, const void* x, const int32_t* topk_idx,
+                          const int32_t* slot_pos, const float* topk_gate,
+                          const void* W1, const void* W3, const void* W2,
+                          const void* residual, double* y /* [n, d] */) {
+#pragma omp parallel
+    {
+        double* h = (double*)malloc(sizeof(double) * (size_t)f);
+        double* ye = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t q = 0; q < n; ++q) {
+            int64_t t = tokens[q];
+            double* yo = y + (size_t)q * d;
+            for (int o = 0; o < d; ++o) yo[o] = 0.0;
+            for (int r = 0; r < k; ++r) {
+                if (slot_pos[(size_t)t * k + r] < 0) continue;
+                int e = topk_idx[(size_t)t * k + r];
+                ffn_row(d, f, act, dtype, x, (size_t)t * d, e, W1, W3, W2, h, ye);
+                for (int o = 0; o < d; ++o) yo[o] += (double)topk_gate[(size_t)t * k + r] * ye[o];
+            }
+            if (residual)
+                for (int o = 0; o < d; ++o) yo[o] += (double)elem(residual, dtype, (size_t)t * d + o);
+        }
+        free(h);
+        free(ye);
+    }
+}

@@ -1,0 +1,398 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+No GPU.  Each test is chosen so that a plausible slip in the oracle (dropped
+term, wrong index or sign, transposed operand, wrong priority) fails it:
+
+* the worked example of the capacity figure ("Expert Parallelism",
+  theinfinity.ai) reproduced exactly, from a fixture under tests/golden;
+* the capacity rule's closed forms for every workload;
+* router logits against exact integer dot products and an fp64 error bound;
+* softmax against a library softmax and the worked example's closed form;
+* top-k and slot assignment against brute-force sorts;
+* the expert FFN and combine against dense evaluation of every expert with
+  library matmuls and activations (dense soft mixture, plain MLP, no drops).
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+import torch.nn.functional as F
+
+import oracle
+from tests.conftest import read_golden
+import moe_inputs
+
+
+# --------------------------------------------------------------------------
+# worked example
+# --------------------------------------------------------------------------
+def _worked_example():
+    rows = read_golden("worked_example.txt")
+    kv = {}
+    choices, dropped = [], []
+    for r in rows:
+        if r[0] == "choice":
+            choices.append((int(r[1]), int(r[2]), int(r[3])))
+        elif r[0] == "dropped":
+            dropped.append((int(r[1]), int(r[2])))
+        else:
+            kv[r[0]] = r[1:]
+    return kv, choices, dropped
+
+
+def test_worked_example_reproduces_caption():
+    kv, choices, dropped = _worked_example()
+    T, d, E, D, k = (int(kv[n][0]) for n in ("T", "d", "E", "D", "k"))
+    c = float(kv["c"][0])
+    x = np.zeros((T, d), np.float32)
+    for t, e0, e1 in choices:
+        x[t, e0] = 3.0
+        x[t, e1] = 2.0
+    Wg = np.eye(E, d, dtype=np.float32)
+    for dt in (torch.float32, torch.bfloat16):
+        xt, wt = torch.from_numpy(x).to(dt), torch.from_numpy(Wg).to(dt)
+        res = oracle.layer_forward(xt, wt, None, None, None, None, k, D, c, oracle.SWIGLU,
+                                   with_ffn=False)
+        s = res.slots
+        assert (s.C, s.C_shard) == (int(kv["C"][0]), int(kv["C_shard"][0]))
+        assert [tuple(r) for r in res.topk_idx.tolist()] == [(e0, e1) for _, e0, e1 in choices]
+        assert s.counts_routed.tolist() == [int(v) for v in kv["counts_routed"]]
+        assert s.counts_kept.tolist() == [int(v) for v in kv["counts_kept"]]
+        unused = [e for e in range(E) if s.counts_routed[e] == 0]
+        assert unused == [int(v) for v in kv["unused_experts"]]
+        got_dropped = sorted((t, r) for t in range(T) for r in range(k) if s.slot_pos[t, r] < 0)
+        assert got_dropped == sorted(dropped)
+        assert s.dropped == 2
+        assert s.expert_offsets.tolist() == [int(v) for v in kv["expert_offsets"]]
+        assert s.shard_offsets.tolist() == [int(v) for v in kv["shard_offsets"]]
+        assert s.shard_routed.tolist() == [int(v) for v in kv["shard_routed"]]
+        assert s.shard_overflow.tolist() == [int(v) for v in kv["shard_overflow"]]
+        np.testing.assert_allclose(res.topk_gate[:, 0], float(kv["gate0"][0]), rtol=0, atol=1e-7)
+        np.testing.assert_allclose(res.topk_gate[:, 1], float(kv["gate1"][0]), rtol=0, atol=1e-7)
+        # the closed form behind the printed gates
+        z = math.exp(3) + math.exp(2) + 6
+        assert abs(res.topk_gate[0, 0] - math.exp(3) / z) < 1e-7
+
+
+# --------------------------------------------------------------------------
+# capacity
+# --------------------------------------------------------------------------
+def test_capacity_closed_forms_of_every_workload():
+    for name, T, k, E, D, c, C, Cs, rm in read_golden("capacities.txt"):
+        wl = moe_inputs.WORKLOADS[name]
+        assert (wl.T, wl.k, wl.E, wl.D) == (int(T), int(k), int(E), int(D))
+        cf = math.inf if c == "inf" else float(c)
+        assert wl.capacity_factor == cf
+        assert oracle.capacity(int(T), int(k), int(E), int(D), cf) == (int(C), int(Cs), int(rm))
+
+
+def test_capacity_edge_cases():
+    # ceil rounds a fractional mean load up; tiny c still gives one slot
+    assert oracle.capacity(6, 2, 8, 4, 1.0)[0] == 2          # 1.5 -> 2
+    assert oracle.capacity(10, 1, 4, 2, 1e-9)[0] == 1
+    # never more than T per expert, never more than T*k per shard
+    assert oracle.capacity(5, 2, 2, 1, 100.0)[:2] == (5, 10)
+    assert oracle.capacity(0, 2, 8, 4, 1.0) == (0, 0, 0)
+    with pytest.raises(ValueError):
+        oracle.capacity(4, 2, 8, 4, 0.0)
+
+
+def test_active_parameter_fraction():
+    # "Expert Parallelism" glossary (inferensys.com): 128 experts, top-2,
+    # about 1.6% of the expert parameters active per token.  Each token reads
+    # the weights of exactly k distinct experts.
+    wl = moe_inputs.Workload("p", T=64, d=16, E=128, D=8, k=2, ffn=16, capacity_factor=math.inf)
+    inp = moe_inputs.make_inputs(wl)
+    _, _, idx, _ = oracle.route(inp.x, inp.Wg, None, wl.k)
+    per_token = np.array([len(set(r)) for r in idx.tolist()])
+    assert (per_token == 2).all()
+    frac = per_token.mean() / wl.E
+    assert frac == 2 / 128 and round(100 * frac, 1) == 1.6
+
+
+# --------------------------------------------------------------------------
+# router
+# --------------------------------------------------------------------------
+def test_logits_exact_on_small_integers():
+    # Every partial sum is an integer below 2^24, so any order is exact: the
+    # oracle must equal the integer dot product (pins operand pairing and bias).
+    rng = np.random.default_rng(11)
+    T, d, E = 37, 96, 13
+    xi = rng.integers(-8, 9, size=(T, d))
+    wi = rng.integers(-8, 9, size=(E, d))
+    b = rng.integers(-50, 51, size=E).astype(np.float32)
+    for dt in (torch.float32, torch.bfloat16):
+        g = oracle.router_logits(torch.tensor(xi, dtype=dt), torch.tensor(wi, dtype=dt),
+                                 torch.from_numpy(b))
+        exact = xi @ wi.T + b.astype(np.int64)
+        assert np.array_equal(g.astype(np.int64), exact)
+        assert np.array_equal(g, exact.astype(np.float32))
+
+
+def test_logits_within_fp32_bound_of_fp64():
+    rng = np.random.default_rng(12)
+    T, d, E = 50, 512, 16
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    w = (rng.standard_normal((E, d)) / math.sqrt(d)).astype(np.float32)
+    g = oracle.router_logits(x, w)
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    bound = d * 2.0**-24 * (np.abs(x).astype(np.float64) @ np.abs(w).astype(np.float64).T)
+    assert (np.abs(g - exact) <= bound).all()
+    # and not trivially: the bound is far below the logit scale
+    assert bound.max() < 1e-3
+
+
+def test_softmax_matches_library_and_sums_to_one():
+    rng = np.random.default_rng(13)
+    g = (3 * rng.standard_normal((200, 64))).astype(np.float32)
+    probs, idx, gate = oracle.softmax_topk(g, 4)
+    ref = scipy.special.softmax(g.astype(np.float64), axis=1)
+    np.testing.assert_allclose(probs, ref, rtol=1e-6, atol=1e-12)
+    np.testing.assert_allclose(probs.astype(np.float64).sum(1), 1.0, atol=1e-6)
+    np.testing.assert_array_equal(gate, np.take_along_axis(probs, idx, 1))
+
+
+def _brute_topk(g, k):
+    # stable sort on (-logit, expert): largest first, equal -> lower index
+    T, E = g.shape
+    out = np.empty((T, k), np.int64)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-float(g[t, e]), e))
+        out[t] = order[:k]
+    return out
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (16, 1), (64, 2), (13, 4), (4, 4)])
+def test_topk_brute_force(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    g = rng.standard_normal((300, E)).astype(np.float32)
+    _, idx, _ = oracle.softmax_topk(g, k)
+    np.testing.assert_array_equal(idx, _brute_topk(g, k))
+
+
+def test_topk_exact_ties_prefer_lower_expert():
+    # x = 0 makes every logit exactly the bias, so ties are exact.
+    E, k, T, d = 12, 3, 20, 8
+    rng = np.random.default_rng(14)
+    bias = rng.integers(0, 3, size=E).astype(np.float32)
+    x = torch.zeros(T, d, dtype=torch.bfloat16)
+    w = torch.from_numpy(rng.standard_normal((E, d)).astype(np.float32)).to(torch.bfloat16)
+    g, _, idx, _ = oracle.route(x, w, torch.from_numpy(bias), k)
+    assert np.array_equal(g, np.broadcast_to(bias, (T, E)))
+    np.testing.assert_array_equal(idx, _brute_topk(g, k))
+    top = sorted(range(E), key=lambda e: (-bias[e], e))[:k]
+    assert idx[0].tolist() == top
+
+
+# --------------------------------------------------------------------------
+# slot assignment
+# --------------------------------------------------------------------------
+def _random_routing(rng, T, E, k, skew=0.0):
+    w = np.exp(-skew * np.log(np.arange(1, E + 1)))
+    w = w / w.sum()
+    idx = np.empty((T, k), np.int32)
+    for t in range(T):
+        idx[t] = rng.choice(E, size=k, replace=False, p=w)
+    return idx
+
+
+def _brute_assign(idx, E, C):
+    # literal sort of all assignments by (expert, rank, token); the first C of
+    # each expert are kept at positions 0..C-1
+    T, k = idx.shape
+    items = sorted(((int(idx[t, r]), r, t) for t in range(T) for r in range(k)))
+    pos = np.full((T, k), -1, np.int64)
+    seen = {}
+    for e, r, t in items:
+        p = seen.get(e, 0)
+        seen[e] = p + 1
+        if p < C:
+            pos[t, r] = p
+    return pos
+
+
+@pytest.mark.parametrize("T,E,D,k,c,skew", [
+    (50, 8, 4, 2, 1.0, 0.0), (64, 8, 4, 2, 1.0, 1.5), (97, 16, 4, 1, 1.25, 2.0),
+    (33, 12, 3, 3, 0.5, 1.0), (40, 4, 2, 4, 1.0, 0.0), (128, 64, 8, 2, 1.0, 1.2)])
+def test_assign_brute_force_and_invariants(T, E, D, k, c, skew):
+    rng = np.random.default_rng(T + E + k)
+    idx = _random_routing(rng, T, E, k, skew)
+    s = oracle.assign(idx, E, D, c)
+    C = s.C
+    np.testing.assert_array_equal(s.slot_pos, _brute_assign(idx, E, C))
+    # counts
+    routed = np.bincount(idx.ravel(), minlength=E)
+    np.testing.assert_array_equal(s.counts_routed, routed)
+    assert s.counts_routed.sum() == T * k
+    assert (s.counts_kept <= C).all()
+    np.testing.assert_array_equal(s.counts_kept, np.minimum(routed, C))
+    kept = int((s.slot_pos >= 0).sum())
+    assert kept + s.dropped == T * k
+    assert kept == s.counts_kept.sum() == s.expert_offsets[E]
+    assert kept <= s.rows_max
+    # per expert, kept positions are exactly 0..kept_e-1
+    for e in range(E):
+        p = sorted(s.slot_pos[idx == e][s.slot_pos[idx == e] >= 0].tolist())
+        assert p == list(range(s.counts_kept[e]))
+    # shard statistics: contiguous blocks of E/D experts
+    per = E // D
+    for sh in range(D):
+        es = range(sh * per, (sh + 1) * per)
+        assert s.shard_routed[sh] == routed[list(es)].sum()
+        assert s.shard_offsets[sh] == s.expert_offsets[sh * per]
+        # assignments dropped on the shard are at least what a shard holding
+        # (E/D)*C slots must refuse
+        dropped_on_shard = sum(int((s.slot_pos[idx == e] < 0).sum()) for e in es)
+        assert dropped_on_shard >= max(0, s.shard_routed[sh] - per * C)
+        if per * C == s.C_shard:
+            # per-expert capacity is at least as strict as the pooled shard one
+            assert dropped_on_shard >= s.shard_overflow[sh]
+    assert s.shard_offsets[D] == kept
+    # row_token inverts (t, r) -> row
+    hit = np.zeros(kept, np.int64)
+    for t in range(T):
+        for r in range(k):
+            if s.slot_pos[t, r] >= 0:
+                row = s.expert_offsets[idx[t, r]] + s.slot_pos[t, r]
+                assert s.row_token[row] == t
+                hit[row] += 1
+    assert (hit == 1).all()
+
+
+def test_priority_rank_before_token():
+    # a kept assignment implies every earlier assignment (rank, then token) to
+    # the same expert is kept too
+    rng = np.random.default_rng(21)
+    idx = _random_routing(rng, 80, 6, 2, 1.0)
+    s = oracle.assign(idx, 6, 3, 0.7)
+    for e in range(6):
+        order = [(r, t) for r in range(2) for t in range(80) if idx[t, r] == e]
+        kept_flags = [s.slot_pos[t, r] >= 0 for r, t in order]
+        assert kept_flags == sorted(kept_flags, reverse=True)
+
+
+def test_more_capacity_never_drops_more():
+    rng = np.random.default_rng(22)
+    idx = _random_routing(rng, 100, 8, 2, 1.5)
+    drops = [oracle.assign(idx, 8, 4, c).dropped for c in (0.25, 0.5, 1.0, 1.25, 2.0, 4.0)]
+    assert drops == sorted(drops, reverse=True)
+    assert oracle.assign(idx, 8, 4, math.inf).dropped == 0
+
+
+def test_shard_overflow_is_the_capacity_formula():
+    # the per-device rule of the capacity paragraph: a device receiving the
+    # fraction p of the T*k assignments overflows by max(0, p*T*k - C_shard)
+    rng = np.random.default_rng(23)
+    T, E, D, k, c = 120, 8, 4, 2, 1.0
+    idx = _random_routing(rng, T, E, k, 2.0)
+    s = oracle.assign(idx, E, D, c)
+    Cs = math.ceil(T * k / D * c)
+    for sh in range(D):
+        p = np.isin(idx, np.arange(sh * E // D, (sh + 1) * E // D)).sum() / (T * k)
+        assert s.shard_overflow[sh] == max(0, round(p * T * k) - Cs)
+
+
+# --------------------------------------------------------------------------
+# dispatch, FFN, combine
+# --------------------------------------------------------------------------
+def test_dispatch_is_the_inverse_permutation():
+    wl = moe_inputs.Workload("d", T=70, d=24, E=8, D=4, k=2, ffn=16, capacity_factor=0.8)
+    inp = moe_inputs.make_inputs(wl)
+    res = oracle.layer_forward(inp.x, inp.Wg, None, inp.W1, inp.W3, inp.W2, wl.k, wl.D,
+                               wl.capacity_factor, oracle.SWIGLU)
+    x16 = inp.x.view(torch.int16).numpy()
+    xd16 = res.xd.view(np.int16)
+    s = res.slots
+    for t in range(wl.T):
+        for r in range(wl.k):
+            if s.slot_pos[t, r] >= 0:
+                row = s.expert_offsets[res.topk_idx[t, r]] + s.slot_pos[t, r]
+                assert np.array_equal(xd16[row], x16[t])
+
+
+def _dense_ffn(x, W1, W3, W2, act):
+    """Every expert on every token with library matmuls: [E, T, d] in fp64."""
+    x = x.double()
+    a = torch.einsum("td,efd->etf", x, W1.double())
+    if act == "swiglu":
+        h = F.silu(a) * torch.einsum("td,efd->etf", x, W3.double())
+    else:
+        h = F.gelu(a)  # exact erf form
+    return torch.einsum("etf,edf->etd", h, W2.double())
+
+
+@pytest.mark.parametrize("dtype,act", [("bf16", "swiglu"), ("f32", "gelu"), ("f32", "swiglu"),
+                                       ("bf16", "gelu")])
+def test_layer_equals_dense_evaluation_without_drops(dtype, act):
+    wl = moe_inputs.Workload("n", T=48, d=32, E=8, D=4, k=2, ffn=40, capacity_factor=math.inf,
+                             dtype=dtype, act=act, seed=5)
+    inp = moe_inputs.make_inputs(wl)
+    res = oracle.layer_forward(inp.x, inp.Wg, None, inp.W1, inp.W3, inp.W2, wl.k, wl.D,
+                               wl.capacity_factor, oracle.act_code(act))
+    assert res.slots.dropped == 0
+    dense = _dense_ffn(inp.x, inp.W1, inp.W3, inp.W2, act).numpy()
+    probs = res.probs.astype(np.float64)
+    want = np.zeros((wl.T, wl.d))
+    for t in range(wl.T):
+        for e in res.topk_idx[t]:
+            want[t] += probs[t, e] * dense[e, t]
+    np.testing.assert_allclose(res.y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_drops_contribute_nothing_and_residual_passes():
+    wl = moe_inputs.Workload("r", T=64, d=16, E=4, D=2, k=2, ffn=24, capacity_factor=0.25,
+                             seed=6, zipf_s=3.0)
+    inp = moe_inputs.make_inputs(wl)
+    resid = torch.randn(wl.T, wl.d, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16)
+    res = oracle.layer_forward(inp.x, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, wl.k, wl.D,
+                               wl.capacity_factor, oracle.SWIGLU, residual=resid)
+    assert res.slots.dropped > 0
+    dense = _dense_ffn(inp.x, inp.W1, inp.W3, inp.W2, "swiglu").numpy()
+    want = resid.double().numpy().copy()
+    all_dropped = 0
+    for t in range(wl.T):
+        kept_any = False
+        for r in range(wl.k):
+            if res.slots.slot_pos[t, r] >= 0:
+                kept_any = True
+                want[t] += float(res.topk_gate[t, r]) * dense[res.topk_idx[t, r], t]
+        all_dropped += not kept_any
+    assert all_dropped > 0  # some tokens pass through the residual only
+    np.testing.assert_allclose(res.y, want, rtol=1e-12, atol=1e-12)
+    # sampled evaluation from the definition agrees with the step-by-step layer
+    toks = [0, 5, 17, 63]
+    y_tok = oracle.token_outputs(toks, inp.x, res.topk_idx, res.slots.slot_pos, res.topk_gate,
+                                 inp.W1, inp.W3, inp.W2, oracle.SWIGLU, residual=resid)
+    np.testing.assert_allclose(y_tok, res.y[toks], rtol=1e-12, atol=1e-12)
+
+
+def test_dense_soft_mixture_when_every_expert_is_chosen():
+    # k = E and no capacity limit: the layer is the dense soft mixture
+    # sum_e p_e FFN_e(x)
+    wl = moe_inputs.Workload("s", T=30, d=16, E=4, D=2, k=4, ffn=20, capacity_factor=math.inf,
+                             dtype="f32", seed=7)
+    inp = moe_inputs.make_inputs(wl)
+    res = oracle.layer_forward(inp.x, inp.Wg, None, inp.W1, inp.W3, inp.W2, wl.k, wl.D,
+                               wl.capacity_factor, oracle.SWIGLU)
+    dense = _dense_ffn(inp.x, inp.W1, inp.W3, inp.W2, "swiglu")
+    p = torch.softmax(inp.x.double() @ inp.Wg.double().T, dim=1)
+    want = torch.einsum("te,etd->td", p, dense).numpy()
+    # the oracle's gates are fp32 (rounded once), the reference's fp64
+    np.testing.assert_allclose(res.y, want, rtol=1e-5, atol=1e-6)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "gelu"])
+def test_single_expert_is_a_plain_mlp(act):
+    wl = moe_inputs.Workload("m", T=25, d=24, E=1, D=1, k=1, ffn=36, capacity_factor=1.0,
+                             dtype="f32", act=act, seed=8)
+    inp = moe_inputs.make_inputs(wl)
+    res = oracle.layer_forward(inp.x, inp.Wg, None, inp.W1, inp.W3, inp.W2, 1, 1, 1.0,
+                               oracle.act_code(act))
+    assert (res.topk_gate == 1.0).all() and res.slots.dropped == 0
+    x = inp.x.double()
+    a = F.linear(x, inp.W1[0].double())
+    h = F.silu(a) * F.linear(x, inp.W3[0].double()) if act == "swiglu" else F.gelu(a)
+    want = F.linear(h, inp.W2[0].double()).numpy()
+    np.testing.assert_allclose(res.y, want, rtol=1e-12, atol=1e-12)
