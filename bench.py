@@ -1,0 +1,423 @@
+"""Benchmark of the single-GPU MoE layer forward (tokens/s on a B300).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one pass of the whole hot path (route, slot assignment, dispatch,
+expert FFN, combine) over one batch of T synthetic tokens of the workload
+(default: the Mixtral-style 8-expert top-2 layer, T=4096, d=1024, ffn=3584,
+c=1.25), inputs and weights resident in HBM.  The L2 cache is flushed
+(a 2 x L2 write) before every timed step, outside the step's events.
+
+Printed (rank 0, one JSON line): tokens/s over the timed steps (max over
+ranks of the device time), the per-call breakdown from a second, identical
+loop that times each C-ABI call with events on the launching stream, the
+roofline of the dominant call (the expert FFN, against the measured bf16
+tensor peak), the end-to-end figure through moe_layer_forward with pinned
+host buffers and the copies inside the timed region, SM clocks sampled
+during the timed loop, and the CPU oracle on a bounded sample.
+
+Multi-GPU (torchrun): every rank runs its own independent layer instance
+(replicas: the layer forward has no cross-GPU exchange here), value = total
+tokens of all ranks / max-over-ranks time, "scaling": "weak".
+
+--impl reference times the CPU oracle (the only reference this method has)
+on the same workload, each step a bounded sample, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs  # noqa: E402
+
+DEFAULT_WORKLOAD = "mixtral_scaled"
+METRIC = "MoE layer forward tokens/sec on 1 B300; % of HBM BW / BF16 tensor peak"
+# dram bytes (read + write) per launch of the expert-FFN call, from the ncu
+# capture summarised in profiles/; None until the current kernels are captured
+FFN_DRAM_BYTES = None
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return pk["hbm_gbs"], pk["bf16_tflops"], "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, 1800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.out.flush()
+        self.out.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our path --
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+    import expert_parallelism_gemm_b300 as moe
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = moe_inputs.WORKLOADS[args.workload]
+    inp = moe_inputs.make_inputs(wl.with_(seed=wl.seed + 1000 * rank), device=dev)
+    p = moe.problem_of(wl)
+    C, C_shard, rows_max = moe.moe_capacity(p)
+    ws = moe.alloc_workspace(p, dev)
+    wsb = ws.numel()
+    y = torch.empty(wl.T, wl.d, dtype=inp.x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def step():
+        moe.moe_layer_forward(p, inp.x, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y, ws, wsb,
+                              stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize(dev)
+    status = moe.moe_device_status(ws, stream)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {moe.moe_status_string(status)}")
+
+    # ---- timed steps (device time, events on the launching stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        for i in range(args.steps):
+            flush()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms_max = float(t.item())
+    status = moe.moe_device_status(ws, stream)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status after timed steps: {moe.moe_status_string(status)}")
+
+    # ---- per-call breakdown: the same step as five C-ABI calls, events between
+    i32, f32 = torch.int32, torch.float32
+    idx = torch.empty(wl.T, wl.k, dtype=i32, device=dev)
+    gate = torch.empty(wl.T, wl.k, dtype=f32, device=dev)
+    slot = torch.empty(wl.T, wl.k, dtype=i32, device=dev)
+    cr, ck = torch.empty(wl.E, dtype=i32, device=dev), torch.empty(wl.E, dtype=i32, device=dev)
+    off = torch.empty(wl.E + 1, dtype=i32, device=dev)
+    so, sr, sov = (torch.empty(n, dtype=i32, device=dev) for n in (wl.D + 1, wl.D, wl.D))
+    row_token = torch.empty(max(rows_max, 1), dtype=i32, device=dev)
+    dropped = torch.empty(1, dtype=i32, device=dev)
+    xd = torch.empty(max(rows_max, 1), wl.d, dtype=inp.x.dtype, device=dev)
+    yd = torch.empty(max(rows_max, 1), wl.d, dtype=inp.x.dtype, device=dev)
+    calls = ["route", "assign", "dispatch", "expert_ffn", "combine"]
+
+    def step_calls(ev=None):
+        if ev: ev[0].record(stream)
+        moe.moe_route(p, inp.x, inp.Wg, inp.bias, idx, gate, None, ws, wsb, stream)
+        if ev: ev[1].record(stream)
+        moe.moe_assign_slots(p, idx, slot, cr, ck, off, so, sr, sov, row_token, dropped, ws, wsb, stream)
+        if ev: ev[2].record(stream)
+        moe.moe_dispatch(p, inp.x, row_token, off, xd, stream)
+        if ev: ev[3].record(stream)
+        moe.moe_expert_ffn(p, xd, off, inp.W1, inp.W3, inp.W2, yd, ws, wsb, stream)
+        if ev: ev[4].record(stream)
+        moe.moe_combine(p, yd, idx, slot, off, gate, None, y, stream)
+        if ev: ev[5].record(stream)
+
+    for _ in range(max(1, args.warmup)):
+        flush()
+        step_calls()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush()
+        step_calls(evs[i])
+    barrier()
+    per_call = {c: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, c in enumerate(calls)}
+    kept = int(off[-1].item())
+    n_dropped = int(dropped.item())
+
+    # ---- end to end through moe_layer_forward with host buffers
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty(wl.T, wl.d, dtype=inp.x.dtype).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_layer_forward(p, x_dev, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y, ws, wsb,
+                              stream)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush()
+        e2e_step()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush()
+        e_s[i].record(stream)
+        e2e_step()
+        e_e[i].record(stream)
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e))
+    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    e2e_ms_max = float(t.item())
+
+    out = None
+    if rank == 0:
+        eb = 2 if wl.dtype == "bf16" else 4
+        hbm_gbs, bf16_tf, peak_src = _peaks()
+        mats = 3 if wl.act == "swiglu" else 2
+        ffn_flops = 2.0 * mats * wl.d * wl.ffn * kept
+        ffn_s = per_call["expert_ffn"] * 1e-3
+        achieved_tf = ffn_flops / ffn_s / 1e12
+        n_exp_used = int((ck > 0).sum().item())
+        route_bytes = wl.T * wl.d * eb + wl.E * wl.d * eb + wl.T * wl.k * 8
+        disp_tokens = int((slot >= 0).any(dim=1).sum().item())
+        dispatch_bytes = disp_tokens * wl.d * eb + kept * wl.d * eb
+        combine_bytes = kept * wl.d * eb + wl.T * wl.d * eb + wl.T * wl.k * 12
+        weight_bytes = mats * wl.d * wl.ffn * eb * n_exp_used
+        gb = lambda b, ms: b / (ms * 1e-3) / 1e9
+        kernels = {
+            "route": {"ms": per_call["route"], "GB_s": gb(route_bytes, per_call["route"]),
+                      "frac_hbm": gb(route_bytes, per_call["route"]) / hbm_gbs},
+            "assign": {"ms": per_call["assign"]},
+            "dispatch": {"ms": per_call["dispatch"], "GB_s": gb(dispatch_bytes, per_call["dispatch"]),
+                         "frac_hbm": gb(dispatch_bytes, per_call["dispatch"]) / hbm_gbs},
+            "expert_ffn": {"ms": per_call["expert_ffn"], "TFLOP_s": achieved_tf,
+                           "frac_bf16": achieved_tf * 1e12 / (bf16_tf * 1e12),
+                           "weight_GB_s": gb(weight_bytes, per_call["expert_ffn"])},
+            "combine": {"ms": per_call["combine"], "GB_s": gb(combine_bytes, per_call["combine"]),
+                        "frac_hbm": gb(combine_bytes, per_call["combine"]) / hbm_gbs},
+        }
+        value = world * wl.T * args.steps / (total_ms_max * 1e-3)
+        clocks = clk.summary()
+        out = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": total_ms_max / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": wl.dtype,
+            "data": "synthetic (seeded torch generator on the device; random-init weights)",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "D": wl.D, "k": wl.k,
+                       "ffn": wl.ffn, "capacity_factor": wl.capacity_factor, "act": wl.act,
+                       "C_expert": C, "kept": kept, "dropped": n_dropped,
+                       "parallelism": f"replicas x{world}", "l2": "flushed before every step (2 x L2 write)"},
+            "roofline": {"kernel": "moe_expert_ffn (tcgen05 gate/up + down GEMMs)", "bound": "tensor",
+                         "achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
+                         "frac": achieved_tf / bf16_tf, "traffic": FFN_DRAM_BYTES,
+                         "peak_source": f"{peak_src} bf16 burst",
+                         "algorithmic": f"2*3*d*ffn flops per kept row x {kept} rows"},
+            "kernels": kernels,
+            "e2e": {"value": world * wl.T * args.steps / (e2e_ms_max * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * eb,
+                    "api": "moe_layer_forward, pinned host x -> device -> host y"},
+            "gpu_launches": args.steps * launches_per_step(wl),
+            "clocks": clocks,
+        }
+    return out
+
+
+def launches_per_step(wl) -> int:
+    """Kernels of one moe_layer_forward: route, count + scan + rank, dispatch,
+    two FFN kernels, combine."""
+    return 1 + 3 + 1 + 2 + 1
+
+
+# -------------------------------------------------------------- oracle --
+def oracle_sample_step(wl, cpu_inp, n_tokens, rng):
+    """One bounded oracle step: routing and slots for all T tokens, then the
+    expert FFN and combine of n_tokens sampled tokens.  Returns
+    (seconds for routing, seconds for the sample, tokens in the sample)."""
+    import oracle
+    t0 = time.perf_counter()
+    g, _, idx, gate = oracle.route(cpu_inp.x, cpu_inp.Wg, cpu_inp.bias, wl.k, want_probs=False)
+    slots = oracle.assign(idx, wl.E, wl.D, wl.capacity_factor)
+    t1 = time.perf_counter()
+    toks = rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False)
+    oracle.token_outputs(toks, cpu_inp.x, idx, slots.slot_pos, gate, cpu_inp.W1, cpu_inp.W3,
+                         cpu_inp.W2, oracle.act_code(wl.act))
+    t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, len(toks)
+
+
+def oracle_tokens_per_s(wl, route_s, sample_s, n):
+    # the whole layer's time: routing of all T tokens plus T/n times the sample
+    return wl.T / (route_s + sample_s * wl.T / n)
+
+
+def oracle_cores():
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n else len(os.sched_getaffinity(0))
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    cpu = moe_inputs.make_inputs(wl, device="cpu")
+    rng = np.random.default_rng(0)
+    r_s, s_s, n = oracle_sample_step(wl, cpu, 16, rng)          # calibrate
+    per_tok = s_s / max(n, 1)
+    n2 = int(max(16, min(wl.T, (budget_s - r_s) / max(per_tok, 1e-6))))
+    r_s, s_s, n = oracle_sample_step(wl, cpu, n2, rng)
+    return {"value": oracle_tokens_per_s(wl, r_s, s_s, n), "unit": "tokens/s", "cores": oracle_cores(),
+            "kind": "oracle",
+            "sample": f"routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random tokens, "
+                      f"extrapolated to {wl.T} ({r_s + s_s:.1f} s of CPU work)"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    wl = moe_inputs.WORKLOADS[args.workload]
+    cpu = moe_inputs.make_inputs(wl, device="cpu")
+    rng = np.random.default_rng(0)
+    r_s, s_s, n = oracle_sample_step(wl, cpu, 8, rng)
+    per_tok = s_s / max(n, 1)
+    n_step = int(max(8, min(wl.T, (6.0 - r_s) / max(per_tok, 1e-6))))  # ~6 s per step
+    for _ in range(args.warmup):
+        oracle_sample_step(wl, cpu, n_step, rng)
+    rs, ss = 0.0, 0.0
+    for _ in range(args.steps):
+        a, b, n = oracle_sample_step(wl, cpu, n_step, rng)
+        rs += a
+        ss += b
+    value = oracle_tokens_per_s(wl, rs / args.steps, ss / args.steps, n)
+    sample = (f"each step: routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random "
+              f"tokens, extrapolated to {wl.T}")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.T / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic (seeded torch generator on the host)",
+            "config": {"workload": wl.name, "T": wl.T, "d": wl.d, "E": wl.E, "k": wl.k, "ffn": wl.ffn,
+                       "capacity_factor": wl.capacity_factor},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_cores(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(moe_inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(moe_inputs.WORKLOADS[args.workload])
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,285 @@
+// api.cu -- the extern "C" boundary declared in include/moe.h: argument
+// validation, the capacity rule, workspace layout, and the launch sequence of
+// the layer forward.  No allocation, no host synchronisation (except in
+// moe_device_status, whose job it is).
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+inline size_t esize(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Capacity rule (theinfinity.ai capacity paragraph, per expert with E in
+// place of D): C = min(T, ceil((T*k/E)*c)); C_shard = min(T*k, ceil((T*k/D)*c)).
+int capacity(const moe_problem* p, int64_t* C, int64_t* Cs, int64_t* rows_max) {
+    const int64_t Tk = p->T * (int64_t)p->k;
+    const double c = p->capacity_factor;
+    if (std::isinf(c)) {
+        *C = p->T;
+        *Cs = Tk;
+    } else {
+        const double ve = std::ceil(((double)Tk / (double)p->E) * c);
+        const double vs = std::ceil(((double)Tk / (double)p->D) * c);
+        *C = ve >= (double)p->T ? p->T : (int64_t)ve;
+        *Cs = vs >= (double)Tk ? Tk : (int64_t)vs;
+    }
+    *rows_max = std::min<int64_t>((int64_t)p->E * *C, Tk);
+    return MOE_OK;
+}
+
+int validate(const moe_problem* p) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (p->T < 0 || p->d < 8 || p->d % 8 || p->ffn < 8 || p->ffn % 8) return MOE_ERR_INVALID_ARG;
+    if (p->E < 1 || p->D < 1 || p->E % p->D) return MOE_ERR_INVALID_ARG;
+    if (p->k < 1 || p->k > p->E) return MOE_ERR_INVALID_ARG;
+    if (!(p->capacity_factor > 0.0)) return MOE_ERR_INVALID_ARG;  // also rejects NaN
+    if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+    if (p->act != MOE_ACT_SWIGLU && p->act != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
+    if (p->E > 256 || p->k > 8) return MOE_ERR_UNSUPPORTED;
+    if (p->T * (int64_t)p->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)p->d * p->ffn >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+int to_problem(const moe_problem* mp, Problem* p) {
+    int rc = validate(mp);
+    if (rc != MOE_OK) return rc;
+    p->T = mp->T;
+    p->d = mp->d;
+    p->E = mp->E;
+    p->D = mp->D;
+    p->k = mp->k;
+    p->ffn = mp->ffn;
+    p->dtype = mp->dtype;
+    p->act = mp->act;
+    capacity(mp, &p->C, &p->C_shard, &p->rows_max);
+    p->nblk = ceil_div(p->T, kAssignBlock);
+    return MOE_OK;
+}
+
+void layout(const Problem& p, moe_workspace_layout* L) {
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + std::max<size_t>(bytes, 1));
+        return at;
+    };
+    const size_t Tk = (size_t)p.T * p.k, eb = esize(p.dtype), rm = (size_t)p.rows_max;
+    L->status = take(4 * sizeof(int32_t));
+    L->topk_idx = take(Tk * 4);
+    L->topk_gate = take(Tk * 4);
+    L->slot_pos = take(Tk * 4);
+    L->counts_routed = take((size_t)p.E * 4);
+    L->counts_kept = take((size_t)p.E * 4);
+    L->expert_offsets = take((size_t)(p.E + 1) * 4);
+    L->shard_offsets = take((size_t)(p.D + 1) * 4);
+    L->shard_routed = take((size_t)p.D * 4);
+    L->shard_overflow = take((size_t)p.D * 4);
+    L->dropped = take(4);
+    L->hist = take((size_t)p.E * p.k * (size_t)p.nblk * 4);
+    L->row_token = take(rm * 4);
+    L->xd = take(rm * p.d * eb);
+    L->h = take(rm * p.ffn * eb);
+    L->yd = take(rm * p.d * eb);
+    L->total = o;
+}
+
+int check_ws(const Problem& p, void* ws, size_t ws_bytes, moe_workspace_layout* L) {
+    layout(p, L);
+    if (!ws || ws_bytes < L->total || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_capacity(const moe_problem* p, int64_t* C_expert, int64_t* C_shard, int64_t* rows_max) {
+    if (!C_expert || !C_shard || !rows_max) return MOE_ERR_INVALID_ARG;
+    int rc = validate(p);
+    if (rc != MOE_OK) return rc;
+    return capacity(p, C_expert, C_shard, rows_max);
+}
+
+int moe_workspace_size(const moe_problem* mp, size_t* bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    moe_workspace_layout L;
+    layout(p, &L);
+    *bytes = L.total;
+    return MOE_OK;
+}
+
+int moe_workspace_layout_of(const moe_problem* mp, moe_workspace_layout* out) {
+    if (!out) return MOE_ERR_INVALID_ARG;
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    layout(p, out);
+    return MOE_OK;
+}
+
+int moe_route(const moe_problem* mp, const void* x, const void* Wg, const float* bias, int32_t* topk_idx,
+              float* topk_gate, float* probs, void* ws, size_t ws_bytes, void* stream) {
+    (void)ws;
+    (void)ws_bytes;
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) return MOE_OK;
+    if (!x || !Wg || !topk_idx || !topk_gate || !aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_route(p, x, Wg, bias, topk_idx, topk_gate, probs, (cudaStream_t)stream));
+}
+
+int moe_assign_slots(const moe_problem* mp, const int32_t* topk_idx, int32_t* slot_pos, int32_t* counts_routed,
+                     int32_t* counts_kept, int32_t* expert_offsets, int32_t* shard_offsets,
+                     int32_t* shard_routed, int32_t* shard_overflow, int32_t* row_token, int32_t* dropped,
+                     void* ws, size_t ws_bytes, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if ((p.T > 0 && (!topk_idx || !slot_pos || !row_token)) || !counts_routed || !counts_kept ||
+        !expert_offsets || !shard_offsets || !shard_routed || !shard_overflow)
+        return MOE_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    int* status = (int*)((char*)ws + L.status);
+    return cuda_rc(launch_assign(p, topk_idx, slot_pos, counts_routed, counts_kept, expert_offsets, shard_offsets,
+                                 shard_routed, shard_overflow, row_token, dropped,
+                                 (int32_t*)((char*)ws + L.hist), status, (cudaStream_t)stream));
+}
+
+int moe_dispatch(const moe_problem* mp, const void* x, const int32_t* row_token, const int32_t* expert_offsets,
+                 void* xd, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.rows_max == 0) return MOE_OK;
+    if (!x || !row_token || !expert_offsets || !xd || !aligned16(x) || !aligned16(xd)) return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_dispatch(p, x, row_token, expert_offsets, xd, (cudaStream_t)stream));
+}
+
+int moe_expert_ffn(const moe_problem* mp, const void* xd, const int32_t* expert_offsets, const void* W1,
+                   const void* W3, const void* W2, void* yd, void* ws, size_t ws_bytes, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!expert_offsets || !W1 || !W2 || !xd || !yd) return MOE_ERR_INVALID_ARG;
+    if (p.act == MOE_ACT_SWIGLU && !W3) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(xd) || !aligned16(yd) || !aligned16(W1) || !aligned16(W2) || (W3 && !aligned16(W3)))
+        return MOE_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    if (p.rows_max == 0) return MOE_OK;
+    void* h = (char*)ws + L.h;
+    int* status = (int*)((char*)ws + L.status);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
+        cudaError_t e = launch_ffn_tc(p, xd, expert_offsets, W1, W3, W2, h, yd, status, s);
+        if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+        return cuda_rc(e);
+    }
+    return cuda_rc(launch_ffn_simt(p, xd, expert_offsets, W1, W3, W2, h, yd, s));
+}
+
+int moe_combine(const moe_problem* mp, const void* yd, const int32_t* topk_idx, const int32_t* slot_pos,
+                const int32_t* expert_offsets, const float* topk_gate, const void* residual, void* y,
+                void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) return MOE_OK;
+    if (!yd || !topk_idx || !slot_pos || !expert_offsets || !topk_gate || !y || !aligned16(yd) ||
+        !aligned16(y) || (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_combine(p, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y,
+                                  (cudaStream_t)stream));
+}
+
+int moe_layer_forward(const moe_problem* mp, const void* x, const void* Wg, const float* bias, const void* W1,
+                      const void* W3, const void* W2, const void* residual, void* y, void* ws, size_t ws_bytes,
+                      void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!x || !Wg || !W1 || !W2 || !y || (p.act == MOE_ACT_SWIGLU && !W3)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W2) || (W3 && !aligned16(W3)) ||
+        !aligned16(y) || (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) return MOE_OK;
+    char* w = (char*)ws;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t* idx = (int32_t*)(w + L.topk_idx);
+    float* gate = (float*)(w + L.topk_gate);
+    int32_t* slot = (int32_t*)(w + L.slot_pos);
+    int32_t* off = (int32_t*)(w + L.expert_offsets);
+    int32_t* row_token = (int32_t*)(w + L.row_token);
+    int* status = (int*)(w + L.status);
+    void *xd = w + L.xd, *h = w + L.h, *yd = w + L.yd;
+
+    cudaError_t e = launch_route(p, x, Wg, bias, idx, gate, nullptr, s);
+    if (e == cudaSuccess)
+        e = launch_assign(p, idx, slot, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
+                          (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
+                          (int32_t*)(w + L.shard_overflow), row_token, (int32_t*)(w + L.dropped),
+                          (int32_t*)(w + L.hist), status, s);
+    if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
+    if (e == cudaSuccess) {
+        if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
+            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, s);
+            if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+        } else {
+            e = launch_ffn_simt(p, xd, off, W1, W3, W2, h, yd, s);
+        }
+    }
+    if (e == cudaSuccess) e = launch_combine(p, yd, idx, slot, off, gate, residual, y, s);
+    return cuda_rc(e);
+}
+
+int moe_device_status(void* ws, void* stream) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    int word = 0;
+    // the status word is the first region of every layout
+    if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (word & kDevTimeout) return MOE_ERR_TIMEOUT;
+    if (word) return MOE_ERR_DEVICE;
+    return MOE_OK;
+}
+
+const char* moe_status_string(int status) {
+    switch (status) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported problem for this build";
+        case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "a kernel's bounded wait timed out";
+        case MOE_ERR_DEVICE: return "a kernel recorded an error (bad index)";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

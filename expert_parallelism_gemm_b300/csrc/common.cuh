@@ -1,0 +1,130 @@
+// common.cuh -- small shared pieces of the CUDA library: element types,
+// vector loads, device status bits and the internal launcher declarations.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Bits OR-ed into the workspace status word by kernels.
+constexpr int kDevTimeout = 1;   // a bounded mbarrier wait gave up
+constexpr int kDevBadIndex = 2;  // an index read from memory was out of range
+
+constexpr int kThreads = 256;
+constexpr int kAssignBlock = 32;  // tokens per slot-assignment block (one warp)
+
+struct Problem {
+    int64_t T;
+    int d, E, D, k, ffn;
+    int dtype, act;
+    int64_t C, C_shard, rows_max;
+    int64_t nblk;  // ceil(T / kAssignBlock)
+};
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// fp32 <-> storage type
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static __device__ __forceinline__ float to_f(float v) { return v; }
+    static __device__ __forceinline__ float from_f(float v) { return v; }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// 16 bytes of a row, as 4 x 32-bit words.
+struct alignas(16) Vec16 {
+    uint32_t w[4];
+};
+
+__device__ __forceinline__ Vec16 ld_nc_v16(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ Vec16 ld_v16(const void* p) {
+    Vec16 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_v16(void* p, const Vec16& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                 "r"(v.w[2]), "r"(v.w[3])
+                 : "memory");
+}
+
+// Unpack 16 bytes into fp32 values: 8 for bf16, 4 for fp32.
+__device__ __forceinline__ void unpack(const Vec16& v, float* out, __nv_bfloat16*) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        out[2 * j] = __uint_as_float(v.w[j] << 16);
+        out[2 * j + 1] = __uint_as_float(v.w[j] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void unpack(const Vec16& v, float* out, float*) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[j] = __uint_as_float(v.w[j]);
+}
+// Pack fp32 values (round to nearest even for bf16).
+__device__ __forceinline__ Vec16 pack(const float* in, __nv_bfloat16*) {
+    Vec16 v;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(in[2 * j], in[2 * j + 1]);
+        v.w[j] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return v;
+}
+__device__ __forceinline__ Vec16 pack(const float* in, float*) {
+    Vec16 v;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v.w[j] = __float_as_uint(in[j]);
+    return v;
+}
+
+template <typename T>
+__host__ __device__ constexpr int vec_elems() {
+    return 16 / (int)sizeof(T);
+}
+
+// ---- launchers (each returns cudaGetLastError() of its launches) ----------
+cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
+                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s);
+
+cudaError_t launch_assign(const Problem& p, const int32_t* topk_idx, int32_t* slot_pos,
+                          int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
+                          int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
+                          int32_t* row_token, int32_t* dropped, int32_t* hist, int* status,
+                          cudaStream_t s);
+
+cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_token,
+                            const int32_t* expert_offsets, void* xd, cudaStream_t s);
+
+cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk_idx,
+                           const int32_t* slot_pos, const int32_t* expert_offsets,
+                           const float* topk_gate, const void* residual, void* y, cudaStream_t s);
+
+cudaError_t launch_ffn_simt(const Problem& p, const void* xd, const int32_t* expert_offsets,
+                            const void* W1, const void* W3, const void* W2, void* h, void* yd,
+                            cudaStream_t s);
+
+// tcgen05 grouped GEMM path (bf16 + SwiGLU). Returns cudaErrorNotSupported
+// when the tensor-map encoder cannot be obtained.
+cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
+                          const void* W1, const void* W3, const void* W2, void* h, void* yd,
+                          int* status, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,538 @@
+// ffn_tc.cu -- expert FFN as a grouped bf16 GEMM on the 5th-generation
+// tensor cores (tcgen05), fed by TMA, accumulating in tensor memory (TMEM).
+//
+// "Expert Parallelism" notes page (narrativegoldmine.com), "Components and
+// Architecture", expert GEMM: the expert's feed-forward network, a standard
+// transformer MLP; formal algorithm, expert computation proportional to the
+// tokens each expert received.  "Expert Parallelism and the All-to-All
+// Bottleneck" (ashishsrivastav.com), phase 3: each device multiplies only the
+// tokens assigned to its local experts.
+//
+// Two launches over the packed, expert-major rows:
+//   gate/up: h[r, :] = silu(xd[r] W1[e]^T) * (xd[r] W3[e]^T)   (SwiGLU fused
+//            into the epilogue: one 128 x 256 accumulator tile holds 128
+//            gate columns and the 128 matching up columns)
+//   down:    yd[r, :] = h[r] W2[e]^T
+// Ragged expert sizes stay on the device: each CTA reads expert_offsets,
+// counts the m-tiles of every expert and walks the tile list
+// (expert, n-tile, m-tile) persistently with stride gridDim.x, so the CTAs
+// running at one time share weight tiles through L2.
+//
+// Per CTA (one per SM, 192 threads):
+//   warp 0   TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage,
+//            128-byte swizzle, 4 stages of 48 KB;
+//   warp 1   TMEM allocation (512 columns = two 128 x 256 fp32
+//            accumulators) and, on one lane, the MMA issuer:
+//            tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, bf16 in,
+//            fp32 accumulate, tcgen05.commit to free a stage / publish a tile;
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//            lanes 32*(w%4)..+31 = the tile's rows), activation, bf16 round,
+//            masked stores of the rows that belong to the tile's expert.
+// Every mbarrier wait is bounded in time; on expiry the kernel records
+// kDevTimeout in the status word, stops issuing work, waits (bounded) for its
+// own copies and MMAs in flight, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;       // rows per tile (MMA M)
+constexpr int BN = 256;       // MMA N (gate/up: 128 + 128 columns)
+constexpr int BK = 64;        // K per stage (one 128-byte swizzle atom of bf16)
+constexpr int UK = 16;        // K per MMA instruction
+constexpr int STAGES = 4;
+constexpr int kTcThreads = 192;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int kMaxE = 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: far above any legitimate wait
+
+// shared-memory map after the 1024-aligned stage area
+struct __align__(8) TcShared {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+    int offs[kMaxE + 1];
+    int tstart[kMaxE + 1];
+};
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(TcShared);
+
+struct TcArgs {
+    int E;
+    int n_tiles;     // n-tiles per expert
+    int k_blocks;    // ceil(K / BK)
+    int n_out;       // output columns (ffn for gate/up, d for down)
+    int wrows;       // weight rows per expert in the flattened [E * wrows, K] map
+    int rows_max;    // rows of the packed A / output buffers
+    const int32_t* expert_offsets;
+    __nv_bfloat16* out;
+    int* status;
+};
+
+// ---------------------------------------------------------------- PTX ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Wait for the phase of `parity` to complete.  Gives up when another role has
+// raised the abort flag or after kTimeoutNs (then raises it and records the
+// timeout).  Returns true when the phase completed.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            atomicOr(status, kDevTimeout);
+            return false;
+        }
+    }
+}
+// Drain wait used on the way out: bounded, ignores the abort flag.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, int* status) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kTimeoutNs) {
+            atomicOr(status, kDevTimeout);
+            return;
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                            int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle,
+// 8-row groups 1024 bytes apart (stride byte offset), leading byte offset
+// unused for swizzled K-major (set to 16 B), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+        " [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Tile -> (expert, m-tile, n-tile).  tstart[e] = first tile of expert e; the
+// largest e with tstart[e] <= tile always has rows (empty experts share the
+// next expert's start).
+__device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int E, int n_tiles, int& e,
+                                            int& mt, int& nt) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (S.tstart[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    e = lo;
+    const int local = tile - S.tstart[e];
+    const int mte = (S.offs[e + 1] - S.offs[e] + BM - 1) / BM;
+    nt = local / mte;
+    mt = local - nt * mte;
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmB3, const TcArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t* stages = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    TcShared& S = *reinterpret_cast<TcShared*>(stages + (size_t)STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = args.E;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);
+            mbar_init(smem_u32(&S.empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&S.tfull[b]), 1);
+            mbar_init(smem_u32(&S.tempty[b]), 4);
+        }
+        mbar_init(smem_u32(&S.drain), 1);
+        S.abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        // expert offsets and per-expert tile starts (warp-wide scan)
+        // offsets must be non-decreasing within [0, rows_max]; otherwise the
+        // kernel records kDevBadIndex and computes nothing
+        const int per = (E + 31) / 32;
+        int loc = 0;
+        bool bad = false;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) {
+                const int o0 = args.expert_offsets[e], o1 = args.expert_offsets[e + 1];
+                bad |= o0 < 0 || o1 < o0 || o1 > args.rows_max;
+                S.offs[e] = o0;
+                loc += (o1 - o0 + BM - 1) / BM * args.n_tiles;
+            }
+        }
+        if (__any_sync(0xffffffffu, bad)) {
+            loc = 0;
+            if (lane == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadIndex);
+        }
+        int incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = incl - loc;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < E) {
+                S.tstart[e] = run;
+                if (loc > 0) {
+                    const int o0 = args.expert_offsets[e], o1 = args.expert_offsets[e + 1];
+                    run += (o1 - o0 + BM - 1) / BM * args.n_tiles;
+                }
+            }
+        }
+        if (lane == 31) {
+            S.tstart[E] = incl;
+            S.offs[E] = args.expert_offsets[E];
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&S.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const int total_tiles = S.tstart[E];
+    const uint32_t tmem_base = S.tmem_base;
+    volatile int* abort_flag = &S.abort_flag;
+    int* status = args.status;
+    const int n_tiles = args.n_tiles, k_blocks = args.k_blocks;
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer --
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued_parity[STAGES];
+        for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+        for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+            int e, mt, nt;
+            tile_coords(tile, S, E, n_tiles, e, mt, nt);
+            const int a_row = S.offs[e] + mt * BM;
+            const int b_row = e * args.wrows + nt * (SWIGLU ? BN / 2 : BN);
+            bool ok = true;
+            for (int kb = 0; kb < k_blocks; ++kb) {
+                if (!wait_phase(smem_u32(&S.empty[stage]), phase ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&S.full[stage]);
+                const uint32_t sa = smem_u32(stages + (size_t)stage * STAGE_BYTES);
+                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
+                if (SWIGLU) {
+                    tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, b_row);
+                    tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB3, fb, kb * BK, b_row);
+                } else {
+                    tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, b_row);
+                }
+                issued_parity[stage] = (int)phase;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
+        // copies still in flight must land before the CTA leaves
+        for (int s = 0; s < STAGES; ++s)
+            if (issued_parity[s] >= 0) drain_phase(smem_u32(&S.full[s]), (uint32_t)issued_parity[s], status);
+    } else if (warp == 1 && lane == 0) {
+        // ------------------------------------------------- MMA issuer --
+        constexpr uint32_t idesc = idesc_bf16(BM, BN);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            if (!wait_phase(smem_u32(&S.tempty[acc]), acc_phase ^ 1u, abort_flag, status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            bool ok = true;
+            for (int kb = 0; kb < k_blocks; ++kb) {
+                if (!wait_phase(smem_u32(&S.full[stage]), phase, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = smem_u32(stages + (size_t)stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk)
+                    mma_bf16(d_tmem, sw128_desc(sa + kk * UK * 2), sw128_desc(sb + kk * UK * 2), idesc,
+                             (kb | kk) != 0);
+                mma_commit(smem_u32(&S.empty[stage]));
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mma_commit(smem_u32(&S.tfull[acc]));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        // every MMA this thread issued has completed once `drain` flips
+        mma_commit(smem_u32(&S.drain));
+        drain_phase(smem_u32(&S.drain), 0, status);
+    } else if (warp >= 2) {
+        // --------------------------------------------------- epilogue --
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row_in_tile = q * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        __nv_bfloat16* out = args.out;
+        const int n_out = args.n_out;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            int e, mt, nt;
+            tile_coords(tile, S, E, n_tiles, e, mt, nt);
+            if (!wait_phase(smem_u32(&S.tfull[acc]), acc_phase, abort_flag, status)) break;
+            tc_fence_after();
+            const int rows_e = S.offs[e + 1] - S.offs[e];
+            const int local_row = mt * BM + row_in_tile;
+            const bool valid = local_row < rows_e;
+            __nv_bfloat16* orow = out + (size_t)(S.offs[e] + local_row) * n_out;
+            const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            if (SWIGLU) {
+                const int col0 = nt * (BN / 2);
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(taddr + c, g);
+                    tmem_ld16(taddr + BN / 2 + c, u);
+                    tmem_ld_wait();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float h2[2];
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            const float a = __uint_as_float(g[2 * j + z]);
+                            const float b = __uint_as_float(u[2 * j + z]);
+                            h2[z] = __fdividef(a, 1.0f + __expf(-a)) * b;
+                        }
+                        pk[j] = pack_bf16x2(h2[0], h2[1]);
+                    }
+                    if (valid) {
+#pragma unroll
+                        for (int v = 0; v < 2; ++v)
+                            if (col0 + c + 8 * v < n_out)
+                                st_v16(orow + col0 + c + 8 * v,
+                                       Vec16{{pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]}});
+                    }
+                }
+            } else {
+                const int col0 = nt * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 16) {
+                    uint32_t a[16];
+                    tmem_ld16(taddr + c, a);
+                    tmem_ld_wait();
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        pk[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+                    if (valid) {
+#pragma unroll
+                        for (int v = 0; v < 2; ++v)
+                            if (col0 + c + 8 * v < n_out)
+                                st_v16(orow + col0 + c + 8 * v,
+                                       Vec16{{pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]}});
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------- host ------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)ptr;
+    }
+    return fn;
+}
+
+// 2-D bf16 map over a row-major [rows, cols] matrix, box [box_rows, 64], 128 B swizzle.
+bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
+                          const void* W1, const void* W3, const void* W2, void* h, void* yd,
+                          int* status, cudaStream_t s) {
+    if (p.rows_max == 0) return cudaSuccess;
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap mA1, mB1, mB3, mA2, mB2;
+    const uint64_t rows = (uint64_t)p.rows_max, E = (uint64_t)p.E;
+    if (!make_map(enc, &mA1, xd, rows, p.d, BM) || !make_map(enc, &mB1, W1, E * p.ffn, p.d, BN / 2) ||
+        !make_map(enc, &mB3, W3, E * p.ffn, p.d, BN / 2) || !make_map(enc, &mA2, h, rows, p.ffn, BM) ||
+        !make_map(enc, &mB2, W2, E * p.d, p.ffn, BN))
+        return cudaErrorInvalidValue;
+
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e1 = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kSmemBytes);
+        cudaError_t e2 = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kSmemBytes);
+        if (e1 != cudaSuccess) return e1;
+        if (e2 != cudaSuccess) return e2;
+        attr_done = true;
+    }
+    // upper bound of m-tiles over all experts: sum_e ceil(n_e / BM) with
+    // sum_e n_e <= rows_max and n_e <= C
+    const int64_t mt_bound = std::min<int64_t>((int64_t)p.E * ceil_div(p.C, BM), ceil_div(p.rows_max, BM) + p.E);
+    const int sms = num_sms();
+
+    TcArgs a1{p.E, (int)ceil_div(p.ffn, BN / 2), (int)ceil_div(p.d, BK), p.ffn, p.ffn, (int)p.rows_max,
+              expert_offsets,
+              (__nv_bfloat16*)h, status};
+    const unsigned g1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(sms, mt_bound * a1.n_tiles));
+    tc_gemm_kernel<true><<<g1, kTcThreads, kSmemBytes, s>>>(mA1, mB1, mB3, a1);
+
+    TcArgs a2{p.E, (int)ceil_div(p.d, BN), (int)ceil_div(p.ffn, BK), p.d, p.d, (int)p.rows_max,
+              expert_offsets,
+              (__nv_bfloat16*)yd, status};
+    const unsigned g2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(sms, mt_bound * a2.n_tiles));
+    tc_gemm_kernel<false><<<g2, kTcThreads, kSmemBytes, s>>>(mA2, mB2, mB2, a2);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,210 @@
+/*
+ * moe.h -- C ABI of the single-GPU forward pass of a capacity-limited top-k
+ * mixture-of-experts (MoE) layer, hand-written CUDA for B300 (sm_103a).
+ *
+ * The layer follows the expert-parallelism pages:
+ *   "Expert Parallelism" notes page (narrativegoldmine.com), sections
+ *     "Components and Architecture" and "Formal Algorithm: Expert
+ *     Parallelism Forward Pass" (gate computation, expert selection, token
+ *     dispatch, expert computation, expert combine, residual addition);
+ *   "Expert Parallelism" (theinfinity.ai, Systems / Distributed), the capacity
+ *     paragraph (C = ceil((B*k/D)*c), overflow max(0, p*B*k - C)) and the
+ *     6-token / 8-expert / 4-device worked example;
+ *   "Expert Parallelism and the All-to-All Bottleneck" (ashishsrivastav.com),
+ *     "The Mechanism of Expert Parallelism", phases 1-4, and "The All-to-All
+ *     Communication Pattern" (contiguous expert-to-device blocks).
+ * The two all-to-all exchanges of the pages become local permutations on one
+ * GPU: dispatch packs kept token rows expert-major (so grouped by the D
+ * logical shards), combine gathers them back to token order.
+ *
+ * Conventions shared by every call:
+ *  - Problem: T tokens of hidden size d, E experts over D shards (E % D == 0,
+ *    shard s holds experts [s*E/D, (s+1)*E/D)), top-k routing, expert FFN
+ *    width ffn, capacity factor c (> 0; +INFINITY = no limit).
+ *  - Memory: every tensor pointer is a DEVICE pointer owned by the caller.
+ *    The library allocates nothing; scratch comes from the caller's workspace
+ *    (moe_workspace_size bytes, zero-filled once before its first use).
+ *    Pointers must be 16-byte aligned; d and ffn must be multiples of 8.
+ *  - Layouts are row-major.  Activations x, xd, yd, y, residual: [rows, d] in
+ *    the layer dtype.  Router weight Wg: [E, d] in the layer dtype, bias: [E]
+ *    fp32.  Expert weights (nn.Linear out x in): W1, W3: [E, ffn, d];
+ *    W2: [E, d, ffn].  topk_idx / slot_pos: [T, k] int32; topk_gate: [T, k]
+ *    fp32; probs: [T, E] fp32.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *    default stream).  Every call is asynchronous and never synchronises.
+ *  - Errors: the return value reports argument validation (nothing is
+ *    launched when it fails) and launch errors.  Errors found by a kernel
+ *    while running (a bounded wait that gave up) are OR-ed into a status word
+ *    in the workspace; moe_device_status() reads and clears it.
+ *  - Determinism: every output is a pure function of the inputs; there are
+ *    no float atomics, and integer outputs do not depend on scheduling.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage dtype of activations and weights. fp32 accumulation everywhere. */
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* Expert FFN form ("a standard transformer MLP per expert", notes page,
+ * "Components and Architecture"):
+ *   SWIGLU: h = silu(x W1^T) * (x W3^T), y = h W2^T
+ *   GELU:   h = gelu_erf(x W1^T),         y = h W2^T   (W3 unused) */
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GELU = 1 } moe_act;
+
+typedef struct {
+    int64_t T;              /* tokens, >= 0, T*k < 2^31                      */
+    int32_t d;              /* hidden size, multiple of 8                     */
+    int32_t E;              /* experts, 1..256                                */
+    int32_t D;              /* logical shards (devices of the pages), E % D == 0 */
+    int32_t k;              /* top-k, 1 <= k <= min(E, 8)                     */
+    int32_t ffn;            /* expert FFN width, multiple of 8                */
+    double capacity_factor; /* c > 0, +INFINITY = never drop                  */
+    int32_t dtype;          /* moe_dtype                                      */
+    int32_t act;            /* moe_act                                        */
+} moe_problem;
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or limit is wrong  */
+    MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what this build supports   */
+    MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed             */
+    MOE_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (device word) */
+    MOE_ERR_DEVICE = 6       /* other error recorded by a kernel              */
+};
+
+/* Byte offsets of the regions of the layer workspace (all 256-byte aligned).
+ * moe_layer_forward leaves every intermediate of the step in its region, so
+ * a caller can read routing results and statistics back from the workspace. */
+typedef struct {
+    size_t status;         /* int32[4]: device error word(s)                 */
+    size_t topk_idx;       /* int32[T*k]                                     */
+    size_t topk_gate;      /* float[T*k]                                     */
+    size_t slot_pos;       /* int32[T*k]                                     */
+    size_t counts_routed;  /* int32[E]                                       */
+    size_t counts_kept;    /* int32[E]                                       */
+    size_t expert_offsets; /* int32[E+1]                                     */
+    size_t shard_offsets;  /* int32[D+1]                                     */
+    size_t shard_routed;   /* int32[D]                                       */
+    size_t shard_overflow; /* int32[D]                                       */
+    size_t dropped;        /* int32[1]: dropped assignments                  */
+    size_t hist;           /* int32 scratch of the slot assignment           */
+    size_t row_token;      /* int32[rows_max]                                */
+    size_t xd;             /* dtype[rows_max * d]: packed expert inputs      */
+    size_t h;              /* dtype[rows_max * ffn]: expert hidden rows      */
+    size_t yd;             /* dtype[rows_max * d]: packed expert outputs     */
+    size_t total;          /* = moe_workspace_size                           */
+} moe_workspace_layout;
+
+/* Capacity rule.  theinfinity.ai capacity paragraph: a device expecting B*k/D
+ * assignments provisions C = ceil((B*k/D)*c); per expert the same rule with E
+ * in place of D (notes page, "Capacity Factor and Token Dropping": c times the
+ * mean load).  Outputs (host pointers, all required):
+ *   *C_expert = min(T, ceil((T*k/E)*c))   (c = inf: T)
+ *   *C_shard  = min(T*k, ceil((T*k/D)*c)) (c = inf: T*k), used for the
+ *               per-shard overflow max(0, routed_s - C_shard)
+ *   *rows_max = min(E*C_expert, T*k), the bound on kept assignments.
+ * Host-only; no CUDA call.  Returns MOE_ERR_INVALID_ARG on a bad problem. */
+int moe_capacity(const moe_problem* p, int64_t* C_expert, int64_t* C_shard,
+                 int64_t* rows_max);
+
+/* Workspace bytes needed by every call of this header for problem *p
+ * (host-only).  *bytes receives the size. */
+int moe_workspace_size(const moe_problem* p, size_t* bytes);
+
+/* Region offsets inside that workspace (host-only). */
+int moe_workspace_layout_of(const moe_problem* p, moe_workspace_layout* out);
+
+/* Router: gate computation and expert selection (notes page, formal
+ * algorithm; ashishsrivastav.com phase 1).
+ *   g[t,e]   = sum_i x[t,i] * Wg[e,i]  (+ bias[e])   fp32, one fused
+ *              multiply-add chain over i ascending from +0, then the bias add
+ *   probs[t] = softmax(g[t])            (temperature 1)
+ *   topk_idx[t, r]  = the expert of rank r (largest logit first; equal logits
+ *                     rank the lower expert first)
+ *   topk_gate[t, r] = probs[t, topk_idx[t, r]]   (not renormalised)
+ * bias and probs may be NULL.  ws is unused (may be NULL). */
+int moe_route(const moe_problem* p, const void* x, const void* Wg, const float* bias,
+              int32_t* topk_idx, float* topk_gate, float* probs,
+              void* ws, size_t ws_bytes, void* stream);
+
+/* Slot assignment and token dropping (notes page, "Capacity Factor and Token
+ * Dropping"; theinfinity.ai capacity paragraph).  Assignments are served in
+ * the priority (rank r, then token t); pos(t, r) counts the earlier
+ * assignments to the same expert; kept iff pos < C_expert.
+ *   slot_pos[t, r]    = pos, or -1 when dropped
+ *   counts_routed[e]  = assignments to e;  counts_kept[e] = min(routed, C)
+ *   expert_offsets    = exclusive scan of counts_kept, E+1 entries
+ *   shard_offsets[s]  = expert_offsets[s*E/D], D+1 entries
+ *   shard_routed[s]   = sum of counts_routed over the shard's experts
+ *   shard_overflow[s] = max(0, shard_routed[s] - C_shard)
+ *   row_token[expert_offsets[e] + pos] = t for every kept (t, r); entries at
+ *                       and beyond expert_offsets[E] are left unwritten
+ *   dropped[0]        = number of dropped assignments (may be NULL)
+ * Uses the workspace's hist region and status word. */
+int moe_assign_slots(const moe_problem* p, const int32_t* topk_idx, int32_t* slot_pos,
+                     int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
+                     int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
+                     int32_t* row_token, int32_t* dropped, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* Dispatch, the pack before the first all-to-all (notes page, token
+ * dispatch; ashishsrivastav.com phase 2), done as a local permutation:
+ *   xd[row] = x[row_token[row]]  for row < expert_offsets[E]
+ * xd has rows_max rows; rows at and beyond expert_offsets[E] are untouched.
+ * Bit-exact byte copy. */
+int moe_dispatch(const moe_problem* p, const void* x, const int32_t* row_token,
+                 const int32_t* expert_offsets, void* xd, void* stream);
+
+/* Expert computation (notes page, expert GEMM and formal algorithm;
+ * ashishsrivastav.com phase 3): for every expert e and every packed row
+ * r in [expert_offsets[e], expert_offsets[e+1]):
+ *   yd[r] = FFN_e(xd[r])   (form set by p->act; fp32 accumulation, the
+ *                           hidden row stored in the layer dtype)
+ * bf16 + SwiGLU runs as a grouped GEMM on the tcgen05 tensor cores (TMA-fed,
+ * accumulators in tensor memory); other forms on a SIMT kernel.
+ * W3 may be NULL for GELU.  Uses the workspace's h region and status word.
+ * Rows at and beyond expert_offsets[E] of yd are untouched. */
+int moe_expert_ffn(const moe_problem* p, const void* xd, const int32_t* expert_offsets,
+                   const void* W1, const void* W3, const void* W2, void* yd,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Combine (notes page, expert combine and residual addition;
+ * ashishsrivastav.com phase 4), back in token order:
+ *   y[t] = sum over r with slot_pos[t,r] >= 0, in rank order, of
+ *          topk_gate[t,r] * yd[expert_offsets[topk_idx[t,r]] + slot_pos[t,r]]
+ *          (+ residual[t])
+ * fp32 accumulation, one rounding to the layer dtype; a token whose every
+ * assignment was dropped gets 0 (+ residual).  residual may be NULL. */
+int moe_combine(const moe_problem* p, const void* yd, const int32_t* topk_idx,
+                const int32_t* slot_pos, const int32_t* expert_offsets,
+                const float* topk_gate, const void* residual, void* y, void* stream);
+
+/* The whole layer forward: route, assign, dispatch, expert FFN, combine, on
+ * one stream, with no host synchronisation.  bias, W3 (GELU) and residual
+ * may be NULL.  Intermediates stay in the workspace regions named by
+ * moe_workspace_layout_of (probs are not produced). */
+int moe_layer_forward(const moe_problem* p, const void* x, const void* Wg, const float* bias,
+                      const void* W1, const void* W3, const void* W2, const void* residual,
+                      void* y, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads the workspace's device status word, clears it
+ * and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if
+ * the synchronisation itself failed). */
+int moe_device_status(void* ws, void* stream);
+
+/* Static English text of a status code. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

@@ -1,0 +1,257 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Every step is checked in isolation -- the CUDA step gets the oracle's result
+of the previous step -- and then the whole layer end to end:
+
+* integer outputs (top-k indices, slot positions, counts, offsets, shard
+  statistics, dropped total, row_token) and the packed rows xd: bit-exact;
+* router probabilities and gates: within 1e-5 relative;
+* bf16 outputs: |a - o| <= 1e-2 + 2e-2 |o| against the fp64 oracle;
+  fp32 outputs: |a - o| <= 1e-5 + 1e-4 |o|.
+
+Small cases run the whole oracle; they span several 128-row and 128/256-column
+tiles with ragged tails, K and N tails (d, ffn not multiples of 64), empty and
+hot experts, C = 1, k = E, k = 8, E = 256, a single token.  The full-size
+workloads check every integer output in full and the FFN / layer output on a
+seeded sample of rows and tokens (first, last, random, and every token with a
+dropped assignment, up to a cap).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import expert_parallelism_gemm_b300 as moe
+import moe_inputs
+import oracle
+from moe_inputs import Workload
+from tests.gpu_steps import (Device, assert_close, assert_probs, host, oracle_dtype_tensor,
+                             oracle_ffn_rows, raw, sample_rows, t_dev)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "ragged_bf16": Workload("ragged_bf16", T=1000, d=256, E=8, D=4, k=2, ffn=384,
+                            capacity_factor=1.0, seed=11),
+    "odd_dims_bf16": Workload("odd_dims_bf16", T=333, d=200, E=8, D=2, k=2, ffn=136,
+                              capacity_factor=1.25, seed=12),
+    "skew_64e_small": Workload("skew_64e_small", T=777, d=128, E=64, D=8, k=2, ffn=192,
+                               capacity_factor=1.0, seed=13, zipf_s=1.2),
+    "top1_128e_small": Workload("top1_128e_small", T=600, d=128, E=128, D=8, k=1, ffn=128,
+                                capacity_factor=1.0, seed=14),
+    "every_expert_k4": Workload("every_expert_k4", T=257, d=64, E=4, D=2, k=4, ffn=64,
+                                capacity_factor=math.inf, seed=15),
+    "one_token": Workload("one_token", T=1, d=64, E=8, D=4, k=2, ffn=64, capacity_factor=1.0,
+                          seed=16),
+    "capacity_one": Workload("capacity_one", T=300, d=64, E=8, D=8, k=2, ffn=64,
+                             capacity_factor=0.01, seed=17),
+    "k8_e16": Workload("k8_e16", T=200, d=64, E=16, D=4, k=8, ffn=64, capacity_factor=1.0, seed=18),
+    "e256": Workload("e256", T=300, d=64, E=256, D=8, k=2, ffn=64, capacity_factor=2.0, seed=19),
+    "hot_expert": Workload("hot_expert", T=700, d=128, E=8, D=4, k=2, ffn=128,
+                           capacity_factor=1.0, seed=22, zipf_s=6.0),
+    "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
+    "fp32_swiglu": Workload("fp32_swiglu", T=200, d=64, E=8, D=4, k=2, ffn=96,
+                            capacity_factor=1.0, dtype="f32", act="swiglu", seed=20),
+    "bf16_gelu": Workload("bf16_gelu", T=200, d=64, E=8, D=4, k=2, ffn=96, capacity_factor=1.0,
+                          dtype="bf16", act="gelu", seed=21),
+}
+FULL = {n: w for n, w in moe_inputs.WORKLOADS.items() if n != "tiny_fp32"}
+
+
+ALL = list(SMALL) + list(FULL)
+# oracle FFN work allowed per sampled check (the oracle runs ~10 GFLOP/s)
+SAMPLE_FLOPS = 4e10
+
+
+def _build_case(name):
+    """Inputs on the GPU and the oracle's routing, slots and packed rows."""
+    wl = SMALL.get(name) or FULL[name]
+    inp = moe_inputs.make_inputs(wl, device="cuda")
+    cpu = inp.to("cpu")
+    g, probs, idx, gate = oracle.route(cpu.x, cpu.Wg, cpu.bias, wl.k)
+    slots = oracle.assign(idx, wl.E, wl.D, wl.capacity_factor)
+    xd = oracle.dispatch(cpu.x, slots.row_token)
+    return name, wl, Device(inp), cpu, dict(logits=g, probs=probs, idx=idx, gate=gate, slots=slots,
+                                            xd=xd)
+
+
+@pytest.fixture(scope="module", params=ALL)
+def case(request):
+    # module scope: pytest runs every test of one workload before the next
+    c = _build_case(request.param)
+    yield c
+    del c
+    torch.cuda.empty_cache()
+
+
+def test_route(case):
+    name, wl, dev, cpu, o = case
+    idx, gate, probs = dev.route(want_probs=True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), o["idx"])
+    assert_probs(gate.cpu().numpy(), o["gate"], "gate")
+    assert_probs(probs.cpu().numpy(), o["probs"], "probs")
+    # without the optional probability output the decisions are the same
+    idx2, gate2, _ = dev.route(want_probs=False)
+    assert torch.equal(idx2, idx) and torch.equal(gate2, gate)
+    assert dev.status() == moe.MOE_OK
+
+
+def test_assign(case):
+    name, wl, dev, cpu, o = case
+    s = o["slots"]
+    out = dev.assign(t_dev(o["idx"]))
+    np.testing.assert_array_equal(out["slot_pos"].cpu().numpy(), s.slot_pos)
+    for key in ("counts_routed", "counts_kept", "expert_offsets", "shard_offsets", "shard_routed",
+                "shard_overflow"):
+        np.testing.assert_array_equal(out[key].cpu().numpy(), getattr(s, key), err_msg=key)
+    assert int(out["dropped"].item()) == s.dropped
+    kept = int(s.expert_offsets[-1])
+    np.testing.assert_array_equal(out["row_token"][:kept].cpu().numpy(), s.row_token)
+    if kept < dev.rows_max:  # rows past the kept ones are left unwritten
+        assert (out["row_token"][kept:] == -7).all()
+    # a second call on the same workspace gives the same answer
+    out2 = dev.assign(t_dev(o["idx"]))
+    assert all(torch.equal(out[k], out2[k]) for k in out)
+    assert dev.status() == moe.MOE_OK
+
+
+def test_dispatch(case):
+    name, wl, dev, cpu, o = case
+    s = o["slots"]
+    kept = int(s.expert_offsets[-1])
+    xd = dev.dispatch(t_dev(s.row_token if kept else np.zeros(1, np.int32)), t_dev(s.expert_offsets))
+    np.testing.assert_array_equal(raw(xd[:kept]), o["xd"])
+    assert (raw(xd[kept:]) == 0).all()  # untouched
+
+
+def _oracle_xd_tensor(o, dev):
+    xd = torch.zeros((max(dev.rows_max, 1), dev.wl.d), dtype=dev.dtype)
+    kept = int(o["slots"].expert_offsets[-1])
+    if kept:
+        src = torch.from_numpy(o["xd"])
+        xd[:kept] = src.view(torch.bfloat16) if dev.dtype == torch.bfloat16 else src
+    return xd.to("cuda")
+
+
+def test_expert_ffn(case):
+    name, wl, dev, cpu, o = case
+    s = o["slots"]
+    kept = int(s.expert_offsets[-1])
+    yd = dev.expert_ffn(_oracle_xd_tensor(o, dev), t_dev(s.expert_offsets))
+    assert dev.status() == moe.MOE_OK
+    act = oracle.act_code(wl.act)
+    if name in SMALL:
+        want = oracle.expert_ffn(o["xd"], s.expert_offsets, cpu.W1, cpu.W3, cpu.W2, act)
+        assert_close(host(yd[:kept]), want, wl.dtype, "yd")
+    else:
+        rng = np.random.default_rng(wl.seed)
+        per_row = 2.0 * wl.d * wl.ffn * (3 if wl.act == "swiglu" else 2)
+        per_expert = int(max(2, min(16, SAMPLE_FLOPS / per_row / wl.E)))
+        rows = sample_rows(s.expert_offsets, per_expert, rng)
+        row_expert = np.searchsorted(s.expert_offsets, rows, side="right") - 1
+        want = oracle_ffn_rows(o["xd"][rows], row_expert, cpu, act, wl)
+        assert_close(host(yd[torch.from_numpy(rows).cuda()]), want, wl.dtype, "yd sample")
+    if kept < dev.rows_max:
+        assert (raw(yd[kept:]) == 0).all()  # rows past the kept ones untouched
+
+
+@pytest.mark.parametrize("with_residual", [False, True])
+def test_combine(case, with_residual):
+    name, wl, dev, cpu, o = case
+    if name not in SMALL:
+        pytest.skip("isolated combine needs the full oracle FFN; covered by the layer check")
+    s = o["slots"]
+    act = oracle.act_code(wl.act)
+    yd_o = oracle.expert_ffn(o["xd"], s.expert_offsets, cpu.W1, cpu.W3, cpu.W2, act)
+    yd_t = oracle_dtype_tensor(yd_o, wl.dtype)          # oracle values in the layer dtype
+    yd_dev = torch.zeros((max(dev.rows_max, 1), wl.d), dtype=dev.dtype, device="cuda")
+    yd_dev[: yd_t.shape[0]] = yd_t
+    resid = None
+    if with_residual:
+        resid = torch.randn(wl.T, wl.d, generator=torch.Generator().manual_seed(99)).to(dev.dtype)
+    y = dev.combine(yd_dev, t_dev(o["idx"]), t_dev(s.slot_pos), t_dev(s.expert_offsets),
+                    t_dev(o["gate"]), None if resid is None else resid.cuda())
+    want = oracle.combine(host(yd_t), o["idx"], s.slot_pos, o["gate"], s.expert_offsets,
+                          resid, oracle.BF16 if wl.dtype == "bf16" else oracle.F32)
+    assert_close(host(y), want, wl.dtype, "y")
+
+
+def _token_sample(wl, slots, rng):
+    """First, last and random tokens, plus tokens with a dropped assignment,
+    within the oracle FFN budget."""
+    per_tok = 2.0 * wl.k * wl.d * wl.ffn * (3 if wl.act == "swiglu" else 2)
+    n = int(max(16, min(1024, SAMPLE_FLOPS / per_tok)))
+    pick = {0, wl.T - 1}
+    pick.update(rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist())
+    dropped_tok = np.nonzero((slots.slot_pos < 0).any(axis=1))[0]
+    if dropped_tok.size:
+        pick.update(rng.choice(dropped_tok, size=min(n // 2 + 1, dropped_tok.size), replace=False).tolist())
+    return np.array(sorted(pick), dtype=np.int64)
+
+
+def test_layer_forward(case):
+    name, wl, dev, cpu, o = case
+    s = o["slots"]
+    act = oracle.act_code(wl.act)
+    resid = None
+    if name in SMALL:
+        resid = torch.randn(wl.T, wl.d, generator=torch.Generator().manual_seed(7)).to(dev.dtype)
+    y = dev.layer(None if resid is None else resid.cuda())
+    assert dev.status() == moe.MOE_OK
+    # intermediates left in the workspace are the oracle's, bit for bit
+    Tk = wl.T * wl.k
+    np.testing.assert_array_equal(dev.region("topk_idx", torch.int32, Tk).cpu().numpy().reshape(wl.T, wl.k),
+                                  o["idx"])
+    np.testing.assert_array_equal(dev.region("slot_pos", torch.int32, Tk).cpu().numpy().reshape(wl.T, wl.k),
+                                  s.slot_pos)
+    np.testing.assert_array_equal(dev.region("expert_offsets", torch.int32, wl.E + 1).cpu().numpy(),
+                                  s.expert_offsets)
+    np.testing.assert_array_equal(dev.region("shard_overflow", torch.int32, wl.D).cpu().numpy(),
+                                  s.shard_overflow)
+    assert int(dev.region("dropped", torch.int32, 1).item()) == s.dropped
+    if name in SMALL:
+        yd_o = oracle.expert_ffn(o["xd"], s.expert_offsets, cpu.W1, cpu.W3, cpu.W2, act)
+        want = oracle.combine(yd_o, o["idx"], s.slot_pos, o["gate"], s.expert_offsets, resid,
+                              oracle.BF16 if wl.dtype == "bf16" else oracle.F32)
+        assert_close(host(y), want, wl.dtype, "y")
+    else:
+        toks = _token_sample(wl, s, np.random.default_rng(1000 + wl.seed))
+        want = oracle.token_outputs(toks, cpu.x, o["idx"], s.slot_pos, o["gate"], cpu.W1, cpu.W3,
+                                    cpu.W2, act)
+        assert_close(host(y[torch.from_numpy(toks).cuda()]), want, wl.dtype, "y sample")
+    # deterministic: a second pass is bit-identical
+    y2 = dev.layer(None if resid is None else resid.cuda())
+    assert torch.equal(y.view(torch.int16) if y.dtype == torch.bfloat16 else y,
+                       y2.view(torch.int16) if y2.dtype == torch.bfloat16 else y2)
+
+
+def test_layer_equals_step_by_step(case):
+    """moe_layer_forward is the composition of the five calls, bit for bit."""
+    name, wl, dev, cpu, o = case
+    if name not in ("ragged_bf16", "skew_64e_small", "tiny_fp32", "mixtral_scaled"):
+        pytest.skip("checked on a few workloads")
+    y = dev.layer()
+    idx, gate, _ = dev.route(want_probs=False)
+    out = dev.assign(idx)
+    xd = dev.dispatch(out["row_token"], out["expert_offsets"])
+    yd = dev.expert_ffn(xd, out["expert_offsets"])
+    y2 = dev.combine(yd, idx, out["slot_pos"], out["expert_offsets"], gate)
+    assert torch.equal(y.view(torch.int32 if y.dtype == torch.float32 else torch.int16),
+                       y2.view(torch.int32 if y2.dtype == torch.float32 else torch.int16))
+
+
+def test_exact_ties_choose_the_lower_expert():
+    # x = 0: every logit is exactly its bias, with ties
+    wl = Workload("ties", T=96, d=64, E=16, D=4, k=3, ffn=64, capacity_factor=1.0, seed=30)
+    inp = moe_inputs.make_inputs(wl, device="cuda")
+    inp.x.zero_()
+    inp.bias = torch.tensor([1, 2, 2, 0, 2, 1, 1, 0, 2, 0, 0, 1, 2, 2, 0, 1], dtype=torch.float32,
+                            device="cuda")
+    dev = Device(inp)
+    idx, gate, _ = dev.route(want_probs=False)
+    assert idx.cpu().tolist() == [[1, 2, 4]] * wl.T
+    _, _, o_idx, _ = oracle.route(inp.x.cpu(), inp.Wg.cpu(), inp.bias.cpu(), wl.k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), o_idx)
