@@ -183,10 +183,13 @@ def combine(yd: np.ndarray, topk_idx, slot_pos, topk_gate, expert_offsets,
     d = yd.shape[1]
     y = np.empty((T, d), dtype=np.float64)
     ra = _host(residual)
-    _load().oracle_combine(T, d, k, dtype, _ptr(idx), _ptr(np.ascontiguousarray(slot_pos, np.int32)),
-                           _ptr(np.ascontiguousarray(topk_gate, np.float32)),
-                           _ptr(np.ascontiguousarray(expert_offsets, np.int32)),
-                           _ptr(np.ascontiguousarray(yd, np.float64)), _ptr(ra), _ptr(y))
+    # converted copies stay referenced here until the C call returns
+    sp = np.ascontiguousarray(slot_pos, np.int32)
+    gt = np.ascontiguousarray(topk_gate, np.float32)
+    eo = np.ascontiguousarray(expert_offsets, np.int32)
+    ydd = np.ascontiguousarray(yd, np.float64)
+    _load().oracle_combine(T, d, k, dtype, _ptr(idx), _ptr(sp), _ptr(gt), _ptr(eo), _ptr(ydd),
+                           _ptr(ra), _ptr(y))
     return y
 
 
@@ -198,10 +201,11 @@ def token_outputs(tokens, x, topk_idx, slot_pos, topk_gate, W1, W3, W2, act: int
     E, f, d = w1.shape
     k = topk_idx.shape[1]
     y = np.empty((toks.shape[0], d), dtype=np.float64)
+    ti = np.ascontiguousarray(topk_idx, np.int32)
+    sp = np.ascontiguousarray(slot_pos, np.int32)
+    gt = np.ascontiguousarray(topk_gate, np.float32)
     _load().oracle_token_outputs(toks.shape[0], _ptr(toks), d, f, k, act, _dtype_code(x),
-                                 _ptr(xa), _ptr(np.ascontiguousarray(topk_idx, np.int32)),
-                                 _ptr(np.ascontiguousarray(slot_pos, np.int32)),
-                                 _ptr(np.ascontiguousarray(topk_gate, np.float32)),
+                                 _ptr(xa), _ptr(ti), _ptr(sp), _ptr(gt),
                                  _ptr(w1), _ptr(w3), _ptr(w2), _ptr(ra), _ptr(y))
     return y
 

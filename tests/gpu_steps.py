@@ -29,8 +29,9 @@ def assert_close(actual, expected, dtype: str, what: str):
     bad = err > atol + rtol * np.abs(o)
     if bad.any():
         i = np.unravel_index(np.argmax(err - (atol + rtol * np.abs(o))), err.shape)
+        where = [tuple(int(v) for v in w) for w in np.argwhere(bad)[:8]]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst at {i}: "
-                             f"got {a[i]!r} want {o[i]!r}")
+                             f"got {a[i]!r} want {o[i]!r}; first bad {where}")
 
 
 def assert_probs(actual, expected, what: str):

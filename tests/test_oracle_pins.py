@@ -396,3 +396,22 @@ def test_single_expert_is_a_plain_mlp(act):
     h = F.silu(a) * F.linear(x, inp.W3[0].double()) if act == "swiglu" else F.gelu(a)
     want = F.linear(h, inp.W2[0].double()).numpy()
     np.testing.assert_allclose(res.y, want, rtol=1e-12, atol=1e-12)
+
+
+def test_combine_converted_inputs_stay_alive():
+    # inputs that need a dtype conversion (fp32 yd, int64 indices, fp64 gates)
+    # must give the same result as inputs passed in the oracle's own dtypes
+    rng = np.random.default_rng(31)
+    T, d, k, E = 64, 32, 2, 8
+    idx = _random_routing(rng, T, E, k)
+    s = oracle.assign(idx, E, 4, 1.0)
+    kept = int(s.expert_offsets[-1])
+    yd64 = rng.standard_normal((kept, d))
+    gate = rng.random((T, k)).astype(np.float32)
+    want = oracle.combine(yd64, idx, s.slot_pos, gate, s.expert_offsets)
+    for _ in range(20):
+        got = oracle.combine(yd64.astype(np.float32), idx.astype(np.int64), s.slot_pos.astype(np.int64),
+                             gate.astype(np.float64), s.expert_offsets.astype(np.int64))
+        np.testing.assert_allclose(got, oracle.combine(yd64.astype(np.float32).astype(np.float64), idx,
+                                                       s.slot_pos, gate, s.expert_offsets), rtol=0, atol=0)
+    np.testing.assert_allclose(want, got, rtol=1e-6, atol=1e-6)
