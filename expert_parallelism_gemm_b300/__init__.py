@@ -28,7 +28,8 @@ MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
 
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe_route",
            "moe_assign_slots", "moe_dispatch", "moe_expert_ffn", "moe_combine",
-           "moe_layer_forward", "moe_device_status", "moe_status_string")
+           "moe_layer_forward", "moe_device_status", "moe_status_string",
+           "moe_assign_slots_static")
 
 
 class moe_problem(ctypes.Structure):
@@ -77,6 +78,7 @@ def load() -> ctypes.CDLL:
     lib.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, sz, P]
     lib.moe_combine.argtypes = [PP, P, P, P, P, P, P, P, P]
     lib.moe_layer_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.moe_assign_slots_static.argtypes = [PP] + [P] * 11
     lib.moe_device_status.argtypes = [P, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
@@ -162,6 +164,19 @@ def moe_assign_slots(problem, topk_idx, slot_pos, counts_routed, counts_kept, ex
                                    _p(row_token), _p(dropped), _p(ws), int(ws_bytes),
                                    _stream(stream)),
            "moe_assign_slots")
+
+
+def moe_assign_slots_static(problem, topk_idx, slot_pos, counts_routed, counts_kept, expert_offsets,
+                            shard_offsets, shard_routed, shard_overflow, row_token, dropped,
+                            stream=None):
+    """moe_assign_slots without a workspace, for callers that cannot allocate
+    device memory; scratch is a static device array shared by all calls (see
+    include/moe.h for its size limit and the rule that overlapping calls race)."""
+    _check(load().moe_assign_slots_static(ctypes.byref(problem), _p(topk_idx), _p(slot_pos),
+                                          _p(counts_routed), _p(counts_kept), _p(expert_offsets),
+                                          _p(shard_offsets), _p(shard_routed), _p(shard_overflow),
+                                          _p(row_token), _p(dropped), _stream(stream)),
+           "moe_assign_slots_static")
 
 
 def moe_dispatch(problem, x, row_token, expert_offsets, xd, stream=None):

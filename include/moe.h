@@ -195,6 +195,29 @@ int moe_layer_forward(const moe_problem* p, const void* x, const void* Wg, const
                       const void* W1, const void* W3, const void* W2, const void* residual,
                       void* y, void* ws, size_t ws_bytes, void* stream);
 
+/* Slot assignment without a workspace, for callers that cannot allocate
+ * device memory (an operator inside a host framework that owns every device
+ * allocation and passes only input and output buffers, or a latency-critical
+ * path that must avoid cudaMalloc's implicit synchronisation).  The pages have
+ * no counterpart of this entry point; it computes exactly what
+ * moe_assign_slots computes, with the same arguments minus the workspace.
+ * Its scratch (histograms, completion ticket, status word) is one file-scope
+ * __device__ array of 4 MiB + 256 B that every GPU loading the library holds
+ * until the process exits.  Limits and rules:
+ *   - accepted only if E * k * ceil(T / 32) <= 1048576; larger problems
+ *     return MOE_ERR_WORKSPACE and launch nothing;
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, once per device, that device current); make that
+ *     first call before any stream capture;
+ *   - all calls share the array and each starts by clearing its ticket and
+ *     status words: calls whose work overlaps on the GPU (other streams, other
+ *     host threads) race and must be serialised by the caller;
+ *   - no cudaMalloc, cudaFree or other allocating call is made. */
+int moe_assign_slots_static(const moe_problem* p, const int32_t* topk_idx, int32_t* slot_pos,
+                            int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
+                            int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
+                            int32_t* row_token, int32_t* dropped, void* stream);
+
 /* Synchronises `stream`, reads the workspace's device status word, clears it
  * and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if
  * the synchronisation itself failed). */
