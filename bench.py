@@ -45,9 +45,11 @@ import moe_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "mixtral_scaled"
 METRIC = "MoE layer forward tokens/sec on 1 B300; % of HBM BW / BF16 tensor peak"
-# dram bytes (read + write) per launch of the expert-FFN call, from the ncu
-# capture summarised in profiles/; None until the current kernels are captured
-FFN_DRAM_BYTES = None
+# dram bytes (read + write) of one expert-FFN call (its two GEMM launches) on
+# the default workload, from the ncu capture summarised in
+# profiles/tc_gemm_mixtral_scaled_full.md; None whenever the kernels have
+# changed since that capture
+FFN_DRAM_BYTES = (134.328064 + 33.003520 + 119.070464 + 3.374336) * 1e6
 
 
 def _peaks():
@@ -292,7 +294,8 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": f"replicas x{world}", "l2": "flushed before every step (2 x L2 write)"},
             "roofline": {"kernel": "moe_expert_ffn (tcgen05 gate/up + down GEMMs)", "bound": "tensor",
                          "achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
-                         "frac": achieved_tf / bf16_tf, "traffic": FFN_DRAM_BYTES,
+                         "frac": achieved_tf / bf16_tf,
+                         "traffic": FFN_DRAM_BYTES if args.workload == DEFAULT_WORKLOAD else None,
                          "peak_source": f"{peak_src} bf16 burst",
                          "algorithmic": f"2*3*d*ffn flops per kept row x {kept} rows"},
             "kernels": kernels,
