@@ -190,30 +190,45 @@ def run_ours(args, rank, world, local_rank):
     xd = torch.empty(max(rows_max, 1), wl.d, dtype=inp.x.dtype, device=dev)
     yd = torch.empty(max(rows_max, 1), wl.d, dtype=inp.x.dtype, device=dev)
     calls = ["route", "assign", "dispatch", "expert_ffn", "combine"]
-
-    def step_calls(ev=None):
-        if ev: ev[0].record(stream)
-        moe.moe_route(p, inp.x, inp.Wg, inp.bias, idx, gate, None, ws, wsb, stream)
-        if ev: ev[1].record(stream)
-        moe.moe_assign_slots(p, idx, slot, cr, ck, off, so, sr, sov, row_token, dropped, ws, wsb, stream)
-        if ev: ev[2].record(stream)
-        moe.moe_dispatch(p, inp.x, row_token, off, xd, stream)
-        if ev: ev[3].record(stream)
-        moe.moe_expert_ffn(p, xd, off, inp.W1, inp.W3, inp.W2, yd, ws, wsb, stream)
-        if ev: ev[4].record(stream)
-        moe.moe_combine(p, yd, idx, slot, off, gate, None, y, stream)
-        if ev: ev[5].record(stream)
-
+    call_fns = [
+        lambda: moe.moe_route(p, inp.x, inp.Wg, inp.bias, idx, gate, None, ws, wsb, None),
+        lambda: moe.moe_assign_slots(p, idx, slot, cr, ck, off, so, sr, sov, row_token, dropped, ws, wsb,
+                                     None),
+        lambda: moe.moe_dispatch(p, inp.x, row_token, off, xd, None),
+        lambda: moe.moe_expert_ffn(p, xd, off, inp.W1, inp.W3, inp.W2, yd, ws, wsb, None),
+        lambda: moe.moe_combine(p, yd, idx, slot, off, gate, None, y, None),
+    ]
     for _ in range(max(1, args.warmup)):
         flush()
-        step_calls()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+        for fn in call_fns:
+            fn()
+    torch.cuda.synchronize(dev)
+    # Each call (stream None: torch's current stream, which is the capture
+    # stream inside torch.cuda.graph) is captured in a CUDA graph of its own and replayed between
+    # events, so the times are the calls' device time (no Python or ctypes
+    # overhead between the events); the calls replay in step order, so every
+    # call reads what the previous one wrote, and L2 is flushed before each.
+    graphs = []
+    for fn in call_fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append(g)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls))] for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
-        flush()
-        step_calls(evs[i])
+        for j, g in enumerate(graphs):
+            flush()
+            evs[i][2 * j].record(stream)
+            g.replay()
+            evs[i][2 * j + 1].record(stream)
     barrier()
-    per_call = {c: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, c in enumerate(calls)}
+    per_call = {c: statistics.mean(e[2 * j].elapsed_time(e[2 * j + 1]) for e in evs)
+                for j, c in enumerate(calls)}
+    status = moe.moe_device_status(ws, stream)
+    if status != moe.MOE_OK:
+        raise RuntimeError(f"device status after the per-call loop: {moe.moe_status_string(status)}")
     kept = int(off[-1].item())
     n_dropped = int(dropped.item())
 
@@ -309,9 +324,9 @@ def run_ours(args, rank, world, local_rank):
 
 
 def launches_per_step(wl) -> int:
-    """Kernels of one moe_layer_forward: route, count + scan + rank, dispatch,
-    two FFN kernels, combine."""
-    return 1 + 3 + 1 + 2 + 1
+    """Kernels of one moe_layer_forward: router with the fused count pass,
+    rank pass, dispatch, two FFN kernels, combine."""
+    return 1 + 1 + 1 + 2 + 1
 
 
 # -------------------------------------------------------------- oracle --

@@ -5,7 +5,7 @@
 #include <algorithm>
 #include <cmath>
 
-#include "common.cuh"
+#include "assign_scan.cuh"
 
 namespace moe {
 namespace {
@@ -234,12 +234,14 @@ int moe_layer_forward(const moe_problem* mp, const void* x, const void* Wg, cons
     int* status = (int*)(w + L.status);
     void *xd = w + L.xd, *h = w + L.h, *yd = w + L.yd;
 
-    cudaError_t e = launch_route(p, x, Wg, bias, idx, gate, nullptr, s);
-    if (e == cudaSuccess)
-        e = launch_assign(p, idx, slot, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
+    int32_t* hist = (int32_t*)(w + L.hist);
+    // router + count pass (status[1] is the count pass's completion ticket), then the rank pass
+    const AssignScan scan{hist, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
                           (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
-                          (int32_t*)(w + L.shard_overflow), row_token, (int32_t*)(w + L.dropped),
-                          (int32_t*)(w + L.hist), status, s);
+                          (int32_t*)(w + L.shard_overflow), (int32_t*)(w + L.dropped),
+                          (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C, p.C_shard};
+    cudaError_t e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
+    if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
     if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
     if (e == cudaSuccess) {
         if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {

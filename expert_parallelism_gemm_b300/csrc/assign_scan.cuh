@@ -1,0 +1,140 @@
+// assign_scan.cuh -- the second half of the slot-assignment count pass, run by
+// whichever CTA of a counting kernel finishes last.
+//
+// "Expert Parallelism" notes page (narrativegoldmine.com), "Capacity Factor
+// and Token Dropping": an expert keeps at most C assignments; "Expert
+// Parallelism" (theinfinity.ai), capacity paragraph: per-device overflow
+// max(0, p*B*k - C_shard), with p*B*k the assignments routed to the device;
+// "Expert Parallelism and the All-to-All Bottleneck" (ashishsrivastav.com):
+// experts sit on devices in contiguous blocks.
+//
+// The counting kernels (the standalone count kernel and the router's fused
+// tail) write hist[e][r][b] = number of rank-r choices of expert e among the
+// tokens of block b (kAssignBlock tokens), then call finish_assign_scan().
+// Every CTA bumps an integer ticket; the last one turns hist into exclusive
+// prefixes in (r, b) order per expert -- the priority order rank first, then
+// token -- and writes the routed and kept counts, expert and shard offsets,
+// shard statistics and the dropped total.  Integer arithmetic only, so the
+// result does not depend on which CTA finishes last.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+struct AssignScan {
+    int32_t* hist;  // [E][k][nblk]; counts in, exclusive prefixes out
+    int32_t* counts_routed;
+    int32_t* counts_kept;
+    int32_t* expert_offsets;
+    int32_t* shard_offsets;
+    int32_t* shard_routed;
+    int32_t* shard_overflow;
+    int32_t* dropped;  // may be null
+    unsigned* ticket;  // zero before the launch; reset to zero by the last CTA
+    int E, D, k;
+    int64_t nblk, C, C_shard;
+};
+
+// Call from every thread of every CTA after the CTA's hist entries are
+// written (no thread may have returned early).  Works for any block size
+// that is a multiple of 32.
+__device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
+    __shared__ bool s_last;
+    __shared__ int s_routed[256];
+    __shared__ int s_kept_off[257];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(a.ticket, 1u) == gridDim.x * gridDim.y * gridDim.z - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int64_t L = (int64_t)a.k * a.nblk;
+    // one warp per expert: exclusive scan of its k * nblk counts, in place,
+    // 256 entries per round (8 contiguous per lane, loads issued together)
+    for (int e = warp; e < a.E; e += nwarps) {
+        int32_t* h = a.hist + (size_t)e * L;
+        int running = 0;
+        for (int64_t base = 0; base < L; base += 256) {
+            const int64_t i0 = base + 8 * lane;
+            int v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = i0 + j < L ? __ldcg(h + i0 + j) : 0;
+            int loc = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) loc += v[j];
+            int incl = loc;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += n;
+            }
+            int run = running + incl - loc;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (i0 + j < L) h[i0 + j] = run;
+                run += v[j];
+            }
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            const int kept = (int)min((int64_t)running, a.C);
+            s_routed[e] = running;
+            s_kept_off[e] = kept;
+            a.counts_routed[e] = running;
+            a.counts_kept[e] = kept;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // expert offsets: exclusive scan of the kept counts (E <= 256)
+        const int per = (a.E + 31) / 32;
+        int loc_kept = 0, loc_drop = 0;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < a.E) {
+                loc_kept += s_kept_off[e];
+                loc_drop += s_routed[e] - s_kept_off[e];
+            }
+        }
+        int incl = loc_kept, drop = loc_drop;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+            drop += __shfl_xor_sync(0xffffffffu, drop, o);
+        }
+        int run = incl - loc_kept;
+        for (int j = 0; j < per; ++j) {
+            const int e = lane * per + j;
+            if (e < a.E) {
+                const int kept = s_kept_off[e];
+                s_kept_off[e] = run;
+                a.expert_offsets[e] = run;
+                run += kept;
+            }
+        }
+        if (lane == 31) {
+            s_kept_off[a.E] = incl;
+            a.expert_offsets[a.E] = incl;
+        }
+        if (lane == 0) {
+            if (a.dropped) a.dropped[0] = drop;
+            *a.ticket = 0u;  // ready for the next call on this scratch
+        }
+    }
+    __syncthreads();
+    const int per = a.E / a.D;
+    for (int s = threadIdx.x; s < a.D; s += blockDim.x) {
+        int64_t rs = 0;
+        for (int q = s * per; q < (s + 1) * per; ++q) rs += s_routed[q];
+        a.shard_routed[s] = (int32_t)rs;
+        a.shard_overflow[s] = (int32_t)(rs > a.C_shard ? rs - a.C_shard : 0);
+        a.shard_offsets[s] = s_kept_off[s * per];
+    }
+    if (threadIdx.x == 0) a.shard_offsets[a.D] = s_kept_off[a.E];
+}
+
+}  // namespace moe

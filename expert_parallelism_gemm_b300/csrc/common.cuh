@@ -104,11 +104,23 @@ __host__ __device__ constexpr int vec_elems() {
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
                          int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s);
 
+// router plus the count pass of the slot assignment (hist and scan outputs in
+// `scan`, defined in assign_scan.cuh); T must be > 0
+struct AssignScan;
+cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
+                               int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
+                               cudaStream_t s);
+
 cudaError_t launch_assign(const Problem& p, const int32_t* topk_idx, int32_t* slot_pos,
                           int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
                           int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
                           int32_t* row_token, int32_t* dropped, int32_t* hist, int* status,
                           cudaStream_t s);
+
+// rank pass alone (the histogram already holds the scanned prefixes)
+cudaError_t launch_rank(const Problem& p, const int32_t* topk_idx, const int32_t* hist,
+                        const int32_t* expert_offsets, int32_t* slot_pos, int32_t* row_token, int* status,
+                        cudaStream_t s);
 
 cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_token,
                             const int32_t* expert_offsets, void* xd, cudaStream_t s);

@@ -12,7 +12,10 @@
 // ranks in ascending order from +0, then the residual, then one rounding.
 //
 // Both are HBM-bound copies: one warp per row or token, each lane moving 16
-// bytes per step, so a warp touches 512 contiguous bytes per instruction.
+// bytes per access, so a warp touches 512 contiguous bytes per instruction.
+// Each lane issues a batch of loads (4 vectors for dispatch; for combine, the
+// k source rows of up to 4 vector columns, plus the residual) before it
+// consumes any, so several loads per lane are in flight.
 #include "common.cuh"
 
 namespace moe {
@@ -26,6 +29,7 @@ dispatch_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restrict_
                 const int32_t* __restrict__ row_token, const int32_t* __restrict__ expert_offsets,
                 T* __restrict__ xd) {
     constexpr int VE = vec_elems<T>();
+    constexpr int B = 4;  // 16-byte loads in flight per lane before the stores
     // rows past rows_max do not exist in xd; a token id outside [0, T) is skipped
     const int64_t rows = min((int64_t)expert_offsets[E], rows_max);
     const int nv = d / VE;
@@ -36,21 +40,33 @@ dispatch_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restrict_
         if (t < 0 || t >= Tn) continue;
         const T* src = x + (size_t)t * d;
         T* dst = xd + (size_t)row * d;
-        for (int v = lane; v < nv; v += 32) st_v16(dst + v * VE, ld_nc_v16(src + v * VE));
+        for (int v0 = lane; v0 < nv; v0 += 32 * B) {
+            Vec16 q[B];
+#pragma unroll
+            for (int j = 0; j < B; ++j)
+                if (v0 + 32 * j < nv) q[j] = ld_nc_v16(src + (v0 + 32 * j) * VE);
+#pragma unroll
+            for (int j = 0; j < B; ++j)
+                if (v0 + 32 * j < nv) st_v16(dst + (v0 + 32 * j) * VE, q[j]);
+        }
     }
 }
 
-template <typename T>
+// CB vector columns per lane per step, each gathering up to 8 / CB ranks, so
+// all of a step's loads are issued before the first multiply-add.
+template <typename T, int CB>
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __restrict__ yd, const int32_t* __restrict__ topk_idx,
-               const int32_t* __restrict__ slot_pos, const int32_t* __restrict__ expert_offsets,
-               const float* __restrict__ topk_gate, const T* __restrict__ residual, T* __restrict__ y) {
+combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __restrict__ yd,
+               const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_pos,
+               const int32_t* __restrict__ expert_offsets, const float* __restrict__ topk_gate,
+               const T* __restrict__ residual, T* __restrict__ y) {
     constexpr int VE = vec_elems<T>();
+    constexpr int KM = 8 / CB;  // ranks this instantiation handles (k <= KM)
     const int nv = d / VE;
     const int lane = threadIdx.x & 31;
     for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < Tn;
          t += (int64_t)gridDim.x * kWarps) {
-        // lane r < k fetches assignment r; broadcast below
+        // lane r < k fetches assignment r; every lane then holds all k
         int64_t my_row = -1;
         float my_gate = 0.0f;
         if (lane < k) {
@@ -62,27 +78,48 @@ combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __res
                 if (my_row >= rows_max) my_row = -1;  // inconsistent input: contributes nothing
             }
         }
-        for (int v = lane; v - lane < nv; v += 32) {
-            float acc[VE];
+        int64_t rows[KM];
+        float gates[KM];
 #pragma unroll
-            for (int j = 0; j < VE; ++j) acc[j] = 0.0f;
-            for (int r = 0; r < k; ++r) {
-                const int64_t row = __shfl_sync(0xffffffffu, my_row, r);
-                const float g = __shfl_sync(0xffffffffu, my_gate, r);
-                if (row < 0 || v >= nv) continue;
-                float vals[8];
-                unpack(ld_nc_v16(yd + (size_t)row * d + v * VE), vals, (T*)nullptr);
+        for (int r = 0; r < KM; ++r) {
+            rows[r] = __shfl_sync(0xffffffffu, my_row, r);
+            gates[r] = __shfl_sync(0xffffffffu, my_gate, r);
+            if (r >= k) rows[r] = -1;
+        }
+        for (int v0 = lane; v0 < nv; v0 += 32 * CB) {
+            Vec16 q[CB][KM];
+            Vec16 rq[CB];
 #pragma unroll
-                for (int j = 0; j < VE; ++j) acc[j] = fmaf(g, vals[j], acc[j]);
+            for (int c = 0; c < CB; ++c) {
+                const int v = v0 + 32 * c;
+#pragma unroll
+                for (int r = 0; r < KM; ++r)
+                    if (rows[r] >= 0 && v < nv) q[c][r] = ld_nc_v16(yd + (size_t)rows[r] * d + v * VE);
+                if (residual && v < nv) rq[c] = ld_nc_v16(residual + (size_t)t * d + v * VE);
             }
-            if (v >= nv) continue;
-            if (residual) {
-                float rv[8];
-                unpack(ld_nc_v16(residual + (size_t)t * d + v * VE), rv, (T*)nullptr);
 #pragma unroll
-                for (int j = 0; j < VE; ++j) acc[j] += rv[j];
+            for (int c = 0; c < CB; ++c) {
+                const int v = v0 + 32 * c;
+                if (v >= nv) continue;
+                float acc[VE];
+#pragma unroll
+                for (int j = 0; j < VE; ++j) acc[j] = 0.0f;
+#pragma unroll
+                for (int r = 0; r < KM; ++r) {
+                    if (rows[r] < 0) continue;
+                    float vals[8];
+                    unpack(q[c][r], vals, (T*)nullptr);
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) acc[j] = fmaf(gates[r], vals[j], acc[j]);
+                }
+                if (residual) {
+                    float rv[8];
+                    unpack(rq[c], rv, (T*)nullptr);
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) acc[j] += rv[j];
+                }
+                st_v16(y + (size_t)t * d + v * VE, pack(acc, (T*)nullptr));
             }
-            st_v16(y + (size_t)t * d + v * VE, pack(acc, (T*)nullptr));
         }
     }
 }
@@ -108,19 +145,34 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_
     return cudaGetLastError();
 }
 
+template <typename T>
+void launch_combine_t(const Problem& p, unsigned g, const void* yd, const int32_t* topk_idx,
+                      const int32_t* slot_pos, const int32_t* expert_offsets, const float* topk_gate,
+                      const void* residual, void* y, cudaStream_t s) {
+    const T* ydt = (const T*)yd;
+    const T* rt = (const T*)residual;
+    T* yt = (T*)y;
+    if (p.k <= 2)
+        combine_kernel<T, 4><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx, slot_pos,
+                                                    expert_offsets, topk_gate, rt, yt);
+    else if (p.k <= 4)
+        combine_kernel<T, 2><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx, slot_pos,
+                                                    expert_offsets, topk_gate, rt, yt);
+    else
+        combine_kernel<T, 1><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx, slot_pos,
+                                                    expert_offsets, topk_gate, rt, yt);
+}
+
 cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk_idx,
                            const int32_t* slot_pos, const int32_t* expert_offsets,
                            const float* topk_gate, const void* residual, void* y, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
     const unsigned g = grid_for(p.T);
     if (p.dtype == MOE_BF16)
-        combine_kernel<__nv_bfloat16><<<g, kThreads, 0, s>>>(
-            p.T, p.rows_max, p.E, p.d, p.k, (const __nv_bfloat16*)yd, topk_idx, slot_pos, expert_offsets, topk_gate,
-            (const __nv_bfloat16*)residual, (__nv_bfloat16*)y);
+        launch_combine_t<__nv_bfloat16>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y,
+                                        s);
     else
-        combine_kernel<float><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, (const float*)yd, topk_idx,
-                                                     slot_pos, expert_offsets, topk_gate,
-                                                     (const float*)residual, (float*)y);
+        launch_combine_t<float>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y, s);
     return cudaGetLastError();
 }
 

@@ -6,190 +6,304 @@
 // (gate weight = probability of the chosen expert); "Components and
 // Architecture": top-k selection and an optional per-expert logit bias.
 //
-// Each logit is one fp32 fused multiply-add chain over the hidden index in
-// ascending order, starting from +0, followed by the bias add.  That order is
-// what makes the top-k decision reproducible bit for bit; any thread may own
-// a (token, expert) pair as long as it keeps the chain's order.
+// Logit order (fixed so that the top-k decision is reproducible bit for bit):
+// the hidden index is dealt into 32 slices of runs of 8 consecutive elements,
+// slice j = { i = 256 m + 8 j + q : q = 0..7 }; each slice sum is one fp32
+// fused multiply-add chain in ascending i from +0; the 32 slice sums are
+// combined by the xor butterfly o = 16, 8, 4, 2, 1 (every slice j replaced by
+// s[j] + s[j ^ o] at once), which leaves the same value in every slice; then
+// the bias is added.
 //
-// Layout: one CTA of 256 threads handles 32 tokens and every expert.  Thread
-// (tg = tid % 32, eg = tid / 32) owns token tg and experts eg, eg+8, ...  The
-// hidden dimension is walked in chunks of 64: x[32 x 64] and Wg[E x 64] are
-// staged to shared memory as fp32 (x rows padded so that the 32 lanes' 16-byte
-// reads of 32 different rows hit distinct banks; Wg rows are read by all 32
-// lanes of a warp at once, a broadcast).  Then one warp per token computes the
-// softmax and the top-k by warp-wide (value, index) reductions.
-#include "common.cuh"
-
+// That order maps onto a warp: lane j owns slice j.  A CTA handles one
+// assignment block of 32 tokens with 8 warps; warp w owns tokens 4w..4w+3
+// and, in pass p, experts 8p..8p+7 -- 32 (token, expert) pairs, so each lane
+// keeps 32 slice sums and every 16-byte shared-memory load feeds 32 (x row) or
+// 64 (Wg row) multiply-adds per lane.  The hidden dimension is walked in
+// chunks of 256 elements (8 per lane) through an S-stage ring of cp.async
+// copies (32 x rows and the pass's 8 Wg rows, in their storage type,
+// zero-filled past T, E and d; a zero element adds an exact zero product).
+// After the last chunk of a pass the warp reduces its 32 pairs with the
+// butterfly in reduce-scatter form: in round o a lane keeps the half of its
+// pairs selected by bit o of its lane index and adds the partner's copy of
+// that half, which is the butterfly's own sum s[j] + s[j ^ o] for those pairs;
+// after five rounds lane j holds pair j.  Passes repeat for every group of 8
+// experts, re-reading x from L2.
+//
+// Softmax and top-k run from a shared-memory logit table: one thread per token
+// for up to 32 experts, one warp per token above that.
+//
+// Inside the layer forward the router also starts the slot assignment: a CTA
+// holds exactly one assignment block of kAssignBlock tokens, so it counts its
+// tokens' rank-r choices per expert (shared-memory integer counts), writes
+// that block's histogram entries, and the last CTA to finish scans them
+// (assign_scan.cuh).  The standalone router call leaves this out.
 #include <math_constants.h>
+
+#include "assign_scan.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kTokPerCta = 32;
-constexpr int kChunk = 64;
-constexpr int kXPitch = kChunk + 4;  // floats
+constexpr int kRT = 4;                       // tokens per warp tile
+constexpr int kRE = 8;                       // experts per warp tile (one pass)
+constexpr int kRouteThreads = 256;           // 8 warps x 4 tokens = 32 tokens
+constexpr int kTok = 32;                     // tokens per CTA
+constexpr int kKC = 256;                     // hidden elements per chunk (32 lanes x 8)
+constexpr int kStageRows = kTok + kRE;       // x rows, then the pass's Wg rows
+static_assert(kTok == kAssignBlock, "one CTA per assignment block");
+static_assert(kRouteThreads / 32 * kRT == kTok, "warp tiles cover the CTA's tokens");
 
-template <typename T, int NE>
-__global__ void __launch_bounds__(kThreads)
-route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x,
-             const T* __restrict__ Wg, const float* __restrict__ bias,
-             int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
-             float* __restrict__ probs) {
-    constexpr int VE = vec_elems<T>();           // elements per 16-byte vector
-    constexpr int kVecPerRow = kChunk / VE;      // vectors per chunk row
-    const int Epad = NE * 8;
-    extern __shared__ __align__(16) float smem[];
-    float* xs = smem;                                   // [32][kXPitch]
-    float* wsm = xs + kTokPerCta * kXPitch;             // [Epad][kChunk]
-    float* lg = wsm + Epad * kChunk;                    // [32][Epad + 1]
-    const int lgp = Epad + 1;
-
-    const int tid = threadIdx.x;
-    const int tg = tid & 31, eg = tid >> 5;
-    const int64_t t0 = (int64_t)blockIdx.x * kTokPerCta;
-
-    float acc[NE];
-#pragma unroll
-    for (int j = 0; j < NE; ++j) acc[j] = 0.0f;
-
-    for (int k0 = 0; k0 < d; k0 += kChunk) {
-        const int n = min(kChunk, d - k0);  // multiple of VE
-        // stage x chunk: 32 rows x kVecPerRow vectors
-        for (int v = tid; v < kTokPerCta * kVecPerRow; v += kThreads) {
-            const int r = v / kVecPerRow, c = (v % kVecPerRow) * VE;
-            float vals[8];
-            if (t0 + r < T_ && c < n) {
-                Vec16 q = ld_nc_v16(x + (size_t)(t0 + r) * d + k0 + c);
-                unpack(q, vals, (T*)nullptr);
-            } else {
-#pragma unroll
-                for (int j = 0; j < VE; ++j) vals[j] = 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < VE; ++j) xs[r * kXPitch + c + j] = vals[j];
-        }
-        // stage Wg chunk: Epad rows
-        for (int v = tid; v < Epad * kVecPerRow; v += kThreads) {
-            const int e = v / kVecPerRow, c = (v % kVecPerRow) * VE;
-            float vals[8];
-            if (e < E && c < n) {
-                Vec16 q = ld_nc_v16(Wg + (size_t)e * d + k0 + c);
-                unpack(q, vals, (T*)nullptr);
-            } else {
-#pragma unroll
-                for (int j = 0; j < VE; ++j) vals[j] = 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < VE; ++j) wsm[e * kChunk + c + j] = vals[j];
-        }
-        __syncthreads();
-        const float* xr = xs + tg * kXPitch;
-        for (int i = 0; i < n; i += 4) {
-            const float4 xv = *reinterpret_cast<const float4*>(xr + i);
-#pragma unroll
-            for (int j = 0; j < NE; ++j) {
-                const float4 wv = *reinterpret_cast<const float4*>(wsm + (eg + 8 * j) * kChunk + i);
-                acc[j] = fmaf(xv.x, wv.x, acc[j]);
-                acc[j] = fmaf(xv.y, wv.y, acc[j]);
-                acc[j] = fmaf(xv.z, wv.z, acc[j]);
-                acc[j] = fmaf(xv.w, wv.w, acc[j]);
-            }
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int j = 0; j < NE; ++j) {
-        const int e = eg + 8 * j;
-        if (e < E) lg[tg * lgp + e] = bias ? acc[j] + bias[e] : acc[j];
-    }
-    __syncthreads();
-
-    // softmax + top-k: warp w handles tokens w, w+8, w+16, w+24
-    const int lane = tid & 31, warp = tid >> 5;
-    constexpr int kMaxPerLane = (NE * 8 + 31) / 32;
-    for (int tt = warp; tt < kTokPerCta; tt += kThreads / 32) {
-        const int64_t t = t0 + tt;
-        if (t >= T_) break;
-        float g[kMaxPerLane];
-        float m = -CUDART_INF_F;
-#pragma unroll
-        for (int q = 0; q < kMaxPerLane; ++q) {
-            const int e = lane + 32 * q;
-            g[q] = e < E ? lg[tt * lgp + e] : -CUDART_INF_F;
-            m = fmaxf(m, g[q]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float s = 0.0f;
-#pragma unroll
-        for (int q = 0; q < kMaxPerLane; ++q)
-            if (lane + 32 * q < E) s += expf(g[q] - m);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        const float inv = 1.0f / s;
-        if (probs) {
-#pragma unroll
-            for (int q = 0; q < kMaxPerLane; ++q) {
-                const int e = lane + 32 * q;
-                if (e < E) probs[(size_t)t * E + e] = expf(g[q] - m) * inv;
-            }
-        }
-        uint32_t taken = 0;
-        for (int r = 0; r < k; ++r) {
-            float bv = -CUDART_INF_F;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int q = 0; q < kMaxPerLane; ++q) {
-                const int e = lane + 32 * q;
-                if (e < E && !(taken >> q & 1u) && (g[q] > bv || be == 0x7fffffff)) {
-                    // within a lane e grows with q, so '>' keeps the lower index on ties
-                    bv = g[q];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            if (lane == 0) {
-                topk_idx[(size_t)t * k + r] = be;
-                topk_gate[(size_t)t * k + r] = expf(bv - m) * inv;
-            }
-        }
-    }
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <typename T, int NE>
-cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
-                           int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s) {
-    const int Epad = NE * 8;
-    const size_t smem =
-        sizeof(float) * ((size_t)kTokPerCta * kXPitch + (size_t)Epad * kChunk + 32 * (Epad + 1));
-    auto kern = route_kernel<T, NE>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
-    const unsigned grid = (unsigned)ceil_div(p.T, kTokPerCta);
-    kern<<<grid, kThreads, smem, s>>>(p.T, p.d, p.E, p.k, (const T*)x, (const T*)Wg, bias, topk_idx,
-                                     topk_gate, probs);
-    return cudaGetLastError();
+// 8 consecutive elements of a shared-memory row, widened to fp32.
+__device__ __forceinline__ void load8(const uint8_t* p, float (&v)[8], __nv_bfloat16*) {
+    unpack(*reinterpret_cast<const Vec16*>(p), v, (__nv_bfloat16*)nullptr);
+}
+__device__ __forceinline__ void load8(const uint8_t* p, float (&v)[8], float*) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 16);
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+
+// One reduce-scatter round of the butterfly over offset O: of the N values
+// a[0..N), keep the half chosen by bit O of the lane and add the partner's.
+template <int O, int N>
+__device__ __forceinline__ void rs_round(float (&a)[32], int lane) {
+    const bool hi = (lane & O) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        const float send = hi ? a[i] : a[i + N / 2];
+        const float keep = hi ? a[i + N / 2] : a[i];
+        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+    }
 }
 
 template <typename T>
-cudaError_t dispatch_ne(const Problem& p, const void* x, const void* Wg, const float* bias,
-                        int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s) {
-    const int ne = (p.E + 7) / 8;
-    if (ne <= 1) return launch_route_t<T, 1>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
-    if (ne <= 2) return launch_route_t<T, 2>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
-    if (ne <= 4) return launch_route_t<T, 4>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
-    if (ne <= 8) return launch_route_t<T, 8>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
-    if (ne <= 16) return launch_route_t<T, 16>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
-    return launch_route_t<T, 32>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
+__host__ __device__ constexpr int route_stages() {
+    return sizeof(T) == 2 ? 4 : 3;
+}
+
+size_t route_smem_bytes(int elem_bytes, int stages, int E, int k) {
+    const int epad = (E + kRE - 1) / kRE * kRE;
+    return (size_t)stages * kStageRows * kKC * elem_bytes + (size_t)kTok * (epad + 1) * sizeof(float) +
+           (size_t)k * E * sizeof(int);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRouteThreads)
+route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
+             const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+             float* __restrict__ topk_gate, float* __restrict__ probs, const AssignScan scan) {
+    constexpr int S = route_stages<T>();
+    constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
+    constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
+    constexpr int VPR = RP / 16;                     // 16-byte vectors per ring row
+
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint8_t* ring = smem;  // [S][kStageRows][RP]
+    const int npass = (E + kRE - 1) / kRE;
+    const int LGP = npass * kRE + 1;
+    float* lg = reinterpret_cast<float*>(smem + (size_t)S * kStageRows * RP);  // [kTok][LGP]
+    int* cnt = reinterpret_cast<int*>(lg + kTok * LGP);                         // [k][E]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * kTok;
+    const int nchunks = (d + kKC - 1) / kKC;
+    const int nq = npass * nchunks;
+    const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+
+    // copies of flattened chunk q = (pass, chunk) into ring slot q % S; always
+    // commits a group
+    auto issue = [&](int q) {
+        if (q < nq) {
+            const int pass = q / nchunks, c = q - pass * nchunks;
+            const int k0 = c * kKC;
+            const uint32_t slot = ring_s + (uint32_t)((q % S) * kStageRows * RP);
+            for (int v = tid; v < kStageRows * VPR; v += kRouteThreads) {
+                const int row = v / VPR, col = (v % VPR) * VE;
+                const bool in_d = k0 + col < d;  // d is a multiple of VE
+                const T* src;
+                bool ok;
+                if (row < kTok) {
+                    ok = in_d && t0 + row < T_;
+                    src = x + (ok ? (size_t)(t0 + row) * d + k0 + col : 0);
+                } else {
+                    const int e = pass * kRE + row - kTok;
+                    ok = in_d && e < E;
+                    src = Wg + (ok ? (size_t)e * d + k0 + col : 0);
+                }
+                cp_async16(slot + (uint32_t)(row * RP + col * (int)sizeof(T)), src, ok ? 16u : 0u);
+            }
+        }
+        cp_async_commit();
+    };
+
+    float acc[32];  // slice sums of pair p = rt * 8 + re
+#pragma unroll
+    for (int p = 0; p < 32; ++p) acc[p] = 0.0f;
+
+#pragma unroll
+    for (int q = 0; q < S - 1; ++q) issue(q);
+    for (int q = 0; q < nq; ++q) {
+        // committed: chunks 0..q+S-2; chunk q must have landed
+        cp_async_wait<S - 2>();
+        __syncthreads();  // chunk q visible; every thread is done with chunk q-1
+        issue(q + S - 1);  // into the slot chunk q-1 used
+        const uint8_t* base = ring + (size_t)(q % S) * kStageRows * RP + lane * 8 * (int)sizeof(T);
+        float xv[kRT][8];
+#pragma unroll
+        for (int rt = 0; rt < kRT; ++rt) load8(base + (size_t)(kRT * warp + rt) * RP, xv[rt], (T*)nullptr);
+#pragma unroll
+        for (int re = 0; re < kRE; ++re) {
+            float wv[8];
+            load8(base + (size_t)(kTok + re) * RP, wv, (T*)nullptr);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+#pragma unroll
+                for (int rt = 0; rt < kRT; ++rt) acc[rt * kRE + re] = fmaf(xv[rt][j], wv[j], acc[rt * kRE + re]);
+        }
+        const int pass = q / nchunks;
+        if (q - pass * nchunks == nchunks - 1) {
+            // end of a pass: butterfly in reduce-scatter form, lane j gets pair j
+            rs_round<16, 32>(acc, lane);
+            rs_round<8, 16>(acc, lane);
+            rs_round<4, 8>(acc, lane);
+            rs_round<2, 4>(acc, lane);
+            rs_round<1, 2>(acc, lane);
+            const int tl = kRT * warp + (lane >> 3);
+            const int e = pass * kRE + (lane & 7);
+            if (e < E) lg[tl * LGP + e] = bias ? acc[0] + bias[e] : acc[0];
+#pragma unroll
+            for (int p = 0; p < 32; ++p) acc[p] = 0.0f;
+        }
+    }
+    cp_async_wait<0>();
+    if (scan.hist)
+        for (int i = tid; i < k * E; i += kRouteThreads) cnt[i] = 0;
+    __syncthreads();
+    const bool count = scan.hist != nullptr;
+
+    if (E <= 32) {
+        // softmax + top-k: one thread per token
+        if (tid < kTok && t0 + tid < T_) {
+            const int64_t t = t0 + tid;
+            const float* gl = lg + tid * LGP;
+            float m = -CUDART_INF_F;
+            for (int e = 0; e < E; ++e) m = fmaxf(m, gl[e]);
+            float s = 0.0f;
+            for (int e = 0; e < E; ++e) s += expf(gl[e] - m);
+            const float inv = 1.0f / s;
+            if (probs)
+                for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = expf(gl[e] - m) * inv;
+            uint32_t taken = 0;
+            for (int r = 0; r < k; ++r) {
+                int be = -1;
+                float bv = -CUDART_INF_F;
+                for (int e = 0; e < E; ++e) {
+                    // ascending e with a strict '>' keeps the lower index on ties
+                    if (!(taken >> e & 1u) && (be < 0 || gl[e] > bv)) {
+                        bv = gl[e];
+                        be = e;
+                    }
+                }
+                taken |= 1u << be;
+                topk_idx[(size_t)t * k + r] = be;
+                topk_gate[(size_t)t * k + r] = expf(bv - m) * inv;
+                if (count) atomicAdd(&cnt[r * E + be], 1);
+            }
+        }
+    } else {
+        // softmax + top-k: one warp per token, lane holds experts lane + 32 q
+        constexpr int kMaxPerLane = 256 / 32;
+        for (int tt = warp; tt < kTok; tt += kRouteThreads / 32) {
+            const int64_t t = t0 + tt;
+            if (t >= T_) break;
+            float gv[kMaxPerLane];
+            float m = -CUDART_INF_F;
+#pragma unroll
+            for (int q = 0; q < kMaxPerLane; ++q) {
+                const int e = lane + 32 * q;
+                gv[q] = e < E ? lg[tt * LGP + e] : -CUDART_INF_F;
+                m = fmaxf(m, gv[q]);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float s = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kMaxPerLane; ++q)
+                if (lane + 32 * q < E) s += expf(gv[q] - m);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            const float inv = 1.0f / s;
+            if (probs) {
+#pragma unroll
+                for (int q = 0; q < kMaxPerLane; ++q) {
+                    const int e = lane + 32 * q;
+                    if (e < E) probs[(size_t)t * E + e] = expf(gv[q] - m) * inv;
+                }
+            }
+            uint32_t taken = 0;
+            for (int r = 0; r < k; ++r) {
+                float bv = -CUDART_INF_F;
+                int be = 0x7fffffff;
+#pragma unroll
+                for (int q = 0; q < kMaxPerLane; ++q) {
+                    const int e = lane + 32 * q;
+                    if (e < E && !(taken >> q & 1u) && (gv[q] > bv || be == 0x7fffffff)) {
+                        // within a lane e grows with q, so '>' keeps the lower index on ties
+                        bv = gv[q];
+                        be = e;
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                if (lane == 0) {
+                    topk_idx[(size_t)t * k + r] = be;
+                    topk_gate[(size_t)t * k + r] = expf(bv - m) * inv;
+                    if (count) atomicAdd(&cnt[r * E + be], 1);
+                }
+            }
+        }
+    }
+    if (count) {
+        __syncthreads();
+        const int64_t b = blockIdx.x;  // this CTA's assignment block
+        for (int i = tid; i < k * E; i += kRouteThreads) {
+            const int e = i / k, r = i % k;
+            scan.hist[((size_t)e * k + r) * scan.nblk + b] = cnt[r * E + e];
+        }
+        finish_assign_scan(scan);
+    }
+}
+
+template <typename T>
+cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
+                           int32_t* topk_idx, float* topk_gate, float* probs, const AssignScan& scan,
+                           cudaStream_t s) {
+    const size_t smem = route_smem_bytes((int)sizeof(T), route_stages<T>(), p.E, p.k);
+    auto kern = route_kernel<T>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const unsigned grid = (unsigned)ceil_div(p.T, kTok);
+    kern<<<grid, kRouteThreads, smem, s>>>(p.T, p.d, p.E, p.k, (const T*)x, (const T*)Wg, bias, topk_idx,
+                                          topk_gate, probs, scan);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -197,9 +311,19 @@ cudaError_t dispatch_ne(const Problem& p, const void* x, const void* Wg, const f
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
                          int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s) {
     if (p.T == 0) return cudaSuccess;
+    AssignScan none{};
     if (p.dtype == MOE_BF16)
-        return dispatch_ne<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
-    return dispatch_ne<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, s);
+        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, none, s);
+    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, none, s);
+}
+
+cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
+                               int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
+                               cudaStream_t s) {
+    if (p.T == 0) return cudaErrorInvalidValue;  // callers handle T = 0 without a launch
+    if (p.dtype == MOE_BF16)
+        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, scan, s);
+    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, scan, s);
 }
 
 }  // namespace moe

@@ -29,7 +29,8 @@
  * Parity status per function (what pins it, see the oracle tests):
  *   oracle_capacity        pinned (closed forms of [TI] and the workloads)
  *   oracle_router_logits   pinned (exact small-integer dot products, fp64
- *                          bound, tie cases)
+ *                          bound, tie cases, a hand-derived rounding case
+ *                          that fixes the slice-and-butterfly order)
  *   oracle_softmax_topk    pinned (worked-example closed form, brute force)
  *   oracle_assign          pinned ([TI] worked example, invariants, brute force)
  *   oracle_dispatch        pinned (inverse permutation property)
@@ -99,9 +100,13 @@ int oracle_capacity(int64_t T, int k, int E, int D, double c,
  * Architecture", gating network: an optional per-expert bias on the logits.
  *
  * Fixed summation order (the pages give none; the top-k decision must be
- * reproducible bit for bit): one fp32 fused multiply-add chain over the
- * hidden index in ascending order, starting from +0:
- *     s = 0; for i = 0..d-1: s = fmaf(x[t,i], Wg[e,i], s);   g = s + b[e]
+ * reproducible bit for bit).  The hidden index is dealt into 32 slices of
+ * runs of 8 consecutive elements: slice j holds i = 256*m + 8*j + q
+ * (m = 0, 1, ...; q = 0..7).  Each slice sum is one fp32 fused multiply-add
+ * chain over its elements in ascending i, starting from +0.  The 32 slice
+ * sums are then combined by a fixed butterfly: for o = 16, 8, 4, 2, 1 every
+ * slice j is replaced, all at once, by s[j] + s[j xor o] (fp32 add); after the
+ * five rounds every s[j] holds the same value, s[0].  Then g = s[0] + b[e].
  * Wg is [E, d] (nn.Linear out x in).
  * ------------------------------------------------------------------------ */
 void oracle_router_logits(int64_t T, int d, int E, int dtype,
@@ -110,12 +115,21 @@ void oracle_router_logits(int64_t T, int d, int E, int dtype,
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         for (int e = 0; e < E; ++e) {
-            float s = 0.0f;
-            for (int i = 0; i < d; ++i)
-                s = fmaf(elem(x, dtype, (size_t)t * d + i),
-                         elem(Wg, dtype, (size_t)e * d + i), s);
-            if (bias) s = s + bias[e];
-            logits[(size_t)t * E + e] = s;
+            float s[32];
+            for (int j = 0; j < 32; ++j) s[j] = 0.0f;
+            for (int i = 0; i < d; ++i) {
+                const int j = (i / 8) % 32;
+                s[j] = fmaf(elem(x, dtype, (size_t)t * d + i),
+                            elem(Wg, dtype, (size_t)e * d + i), s[j]);
+            }
+            for (int o = 16; o >= 1; o /= 2) {
+                float n[32];
+                for (int j = 0; j < 32; ++j) n[j] = s[j] + s[j ^ o];
+                for (int j = 0; j < 32; ++j) s[j] = n[j];
+            }
+            float g = s[0];
+            if (bias) g = g + bias[e];
+            logits[(size_t)t * E + e] = g;
         }
     }
 }

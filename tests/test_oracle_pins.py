@@ -144,6 +144,36 @@ def test_logits_within_fp32_bound_of_fp64():
     assert bound.max() < 1e-3
 
 
+def test_logit_order_rounding_cases_derived_by_hand():
+    # The summation order is a reading (the pages give none): 32 slices of
+    # runs of 8 consecutive hidden elements (slice j: i = 256m + 8j + q), one
+    # ascending fmaf chain per slice from +0, then the xor butterfly over
+    # o = 16, 8, 4, 2, 1.  These inputs make fp32 rounding depend on the order,
+    # and the expected values were worked out by hand from that definition.
+    d = 256
+    # (a) slice 0 holds 2^12 * 2^12 = 2^24, slices 1..31 hold 1 each (at
+    # i = 8j).  Butterfly: round 16: 2^24 + 1 -> 2^24 (ties to even), every
+    # other slice pair -> 2; round 8: 2^24 + 2; round 4: + 4; round 2: + 8;
+    # round 1: + 16.  Result 2^24 + 30.  (One ascending chain would give 2^24,
+    # slices of single elements i mod 32 would give 2^24 + 24.)
+    x = np.zeros((1, d), np.float32)
+    w = np.zeros((1, d), np.float32)
+    x[0, 0] = w[0, 0] = 2.0**12
+    for j in range(1, 32):
+        x[0, 8 * j] = w[0, 8 * j] = 1.0
+    # (b) within one slice the chain is ascending: products 1, 1, 2^24 at
+    # i = 0, 1, 2 give 1, 2, 2^24 + 2 (exact); descending would give 2^24.
+    x2 = np.zeros((1, d), np.float32)
+    w2 = np.zeros((1, d), np.float32)
+    x2[0, 0] = w2[0, 0] = x2[0, 1] = w2[0, 1] = 1.0
+    x2[0, 2] = w2[0, 2] = 2.0**12
+    for dt in (torch.float32, torch.bfloat16):
+        g = oracle.router_logits(torch.tensor(x, dtype=dt), torch.tensor(w, dtype=dt))
+        assert float(g[0, 0]) == 16777246.0
+        g2 = oracle.router_logits(torch.tensor(x2, dtype=dt), torch.tensor(w2, dtype=dt))
+        assert float(g2[0, 0]) == 16777218.0
+
+
 def test_softmax_matches_library_and_sums_to_one():
     rng = np.random.default_rng(13)
     g = (3 * rng.standard_normal((200, 64))).astype(np.float32)
