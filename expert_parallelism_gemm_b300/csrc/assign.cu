@@ -50,6 +50,8 @@ __device__ __forceinline__ int load_expert(const int32_t* idx, int64_t t, int r,
 __global__ void __launch_bounds__(kThreads)
 count_kernel(int64_t T, int E, int k, int64_t nblk, const int32_t* __restrict__ idx, AssignScan a,
              int* status) {
+    dep_wait();
+    dep_release();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int r = blockIdx.y;
@@ -67,6 +69,8 @@ __global__ void __launch_bounds__(kThreads)
 rank_kernel(int64_t T, int E, int k, int64_t nblk, int64_t C, const int32_t* __restrict__ idx,
             const int32_t* __restrict__ hist, const int32_t* __restrict__ expert_offsets,
             int32_t* __restrict__ slot_pos, int32_t* __restrict__ row_token, int* status) {
+    dep_wait();
+    dep_release();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int r = blockIdx.y;
@@ -98,8 +102,7 @@ cudaError_t launch_assign(const Problem& p, const int32_t* topk_idx, int32_t* sl
                        p.C_shard};
     // at least one CTA, so that T = 0 still writes zero counts and offsets
     const dim3 grid((unsigned)std::max<int64_t>(1, ceil_div(p.nblk, kThreads / 32)), (unsigned)p.k);
-    count_kernel<<<grid, kThreads, 0, s>>>(p.T, p.E, p.k, p.nblk, topk_idx, a, status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_k(count_kernel, grid, dim3(kThreads), 0, s, p.T, p.E, p.k, p.nblk, topk_idx, a, status);
     if (e != cudaSuccess || p.nblk == 0) return e;
     return launch_rank(p, topk_idx, hist, expert_offsets, slot_pos, row_token, status, s);
 }
@@ -109,9 +112,8 @@ cudaError_t launch_rank(const Problem& p, const int32_t* topk_idx, const int32_t
                         cudaStream_t s) {
     if (p.nblk == 0) return cudaSuccess;
     const dim3 grid((unsigned)ceil_div(p.nblk, kThreads / 32), (unsigned)p.k);
-    rank_kernel<<<grid, kThreads, 0, s>>>(p.T, p.E, p.k, p.nblk, p.C, topk_idx, hist, expert_offsets,
-                                          slot_pos, row_token, status);
-    return cudaGetLastError();
+    return launch_k(rank_kernel, grid, dim3(kThreads), 0, s, p.T, p.E, p.k, p.nblk, p.C, topk_idx, hist,
+                    expert_offsets, slot_pos, row_token, status);
 }
 
 }  // namespace moe

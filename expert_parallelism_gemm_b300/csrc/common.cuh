@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -98,6 +100,32 @@ __device__ __forceinline__ Vec16 pack(const float* in, float*) {
 template <typename T>
 __host__ __device__ constexpr int vec_elems() {
     return 16 / (int)sizeof(T);
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// launch_k(), which lets the next kernel on the stream be scheduled while the
+// previous one drains, and every kernel calls dep_wait() -- which returns once
+// all earlier work on the stream has completed and is visible -- before its
+// first global-memory access, then dep_release() so that the kernel after it
+// may be scheduled.  Only setup that touches no global memory (shared-memory
+// barriers, tensor-memory allocation) comes before dep_wait().
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void dep_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ---- launchers (each returns cudaGetLastError() of its launches) ----------

@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kThreads)
 ffn_simt_kernel(int N, int K, int64_t rows_max, const T* __restrict__ A,
                 const int32_t* __restrict__ expert_offsets, const T* __restrict__ B,
                 const T* __restrict__ B3, T* __restrict__ out) {
+    dep_wait();
+    dep_release();
     const int e = blockIdx.z;
     const int64_t r0 = (int64_t)expert_offsets[e] + (int64_t)blockIdx.x * BM;
     // rows never reach past rows_max, whatever the offsets say
@@ -91,16 +93,17 @@ cudaError_t launch_t(const Problem& p, const void* xd, const int32_t* off, const
                      const void* W3, const void* W2, void* h, void* yd, cudaStream_t s) {
     const unsigned mt = (unsigned)ceil_div(p.C, BM);
     const dim3 g1(mt, (unsigned)ceil_div(p.ffn, BN), (unsigned)p.E);
+    cudaError_t err;
     if (p.act == MOE_ACT_SWIGLU)
-        ffn_simt_kernel<T, kSwiGLU><<<g1, kThreads, 0, s>>>(p.ffn, p.d, p.rows_max, (const T*)xd, off,
-                                                           (const T*)W1, (const T*)W3, (T*)h);
+        err = launch_k(ffn_simt_kernel<T, kSwiGLU>, g1, dim3(kThreads), 0, s, p.ffn, p.d, p.rows_max,
+                       (const T*)xd, off, (const T*)W1, (const T*)W3, (T*)h);
     else
-        ffn_simt_kernel<T, kGeLU><<<g1, kThreads, 0, s>>>(p.ffn, p.d, p.rows_max, (const T*)xd, off,
-                                                         (const T*)W1, nullptr, (T*)h);
+        err = launch_k(ffn_simt_kernel<T, kGeLU>, g1, dim3(kThreads), 0, s, p.ffn, p.d, p.rows_max,
+                       (const T*)xd, off, (const T*)W1, (const T*)nullptr, (T*)h);
+    if (err != cudaSuccess) return err;
     const dim3 g2(mt, (unsigned)ceil_div(p.d, BN), (unsigned)p.E);
-    ffn_simt_kernel<T, kPlain><<<g2, kThreads, 0, s>>>(p.d, p.ffn, p.rows_max, (const T*)h, off,
-                                                      (const T*)W2, nullptr, (T*)yd);
-    return cudaGetLastError();
+    return launch_k(ffn_simt_kernel<T, kPlain>, g2, dim3(kThreads), 0, s, p.d, p.ffn, p.rows_max, (const T*)h,
+                    off, (const T*)W2, (const T*)nullptr, (T*)yd);
 }
 
 }  // namespace

@@ -230,6 +230,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&S.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // global memory only from here on (earlier kernels on the stream are done)
+    dep_wait();
+    dep_release();
     if (warp == 0) {
         // expert offsets and per-expert tile starts (warp-wide scan)
         // offsets must be non-decreasing within [0, rows_max]; otherwise the
@@ -271,13 +281,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             S.tstart[E] = incl;
             S.offs[E] = args.expert_offsets[E];
         }
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&S.tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
@@ -525,14 +528,14 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
               expert_offsets,
               (__nv_bfloat16*)h, status};
     const unsigned g1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(sms, mt_bound * a1.n_tiles));
-    tc_gemm_kernel<true><<<g1, kTcThreads, kSmemBytes, s>>>(mA1, mB1, mB3, a1);
+    cudaError_t err = launch_k(tc_gemm_kernel<true>, dim3(g1), dim3(kTcThreads), kSmemBytes, s, mA1, mB1, mB3, a1);
+    if (err != cudaSuccess) return err;
 
     TcArgs a2{p.E, (int)ceil_div(p.d, BN), (int)ceil_div(p.ffn, BK), p.d, p.d, (int)p.rows_max,
               expert_offsets,
               (__nv_bfloat16*)yd, status};
     const unsigned g2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(sms, mt_bound * a2.n_tiles));
-    tc_gemm_kernel<false><<<g2, kTcThreads, kSmemBytes, s>>>(mA2, mB2, mB2, a2);
-    return cudaGetLastError();
+    return launch_k(tc_gemm_kernel<false>, dim3(g2), dim3(kTcThreads), kSmemBytes, s, mA2, mB2, mB2, a2);
 }
 
 }  // namespace moe

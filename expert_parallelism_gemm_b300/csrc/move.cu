@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kThreads)
 dispatch_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restrict__ x,
                 const int32_t* __restrict__ row_token, const int32_t* __restrict__ expert_offsets,
                 T* __restrict__ xd) {
+    dep_wait();
+    dep_release();
     constexpr int VE = vec_elems<T>();
     constexpr int B = 4;  // 16-byte loads in flight per lane before the stores
     // rows past rows_max do not exist in xd; a token id outside [0, T) is skipped
@@ -60,6 +62,8 @@ combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __res
                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_pos,
                const int32_t* __restrict__ expert_offsets, const float* __restrict__ topk_gate,
                const T* __restrict__ residual, T* __restrict__ y) {
+    dep_wait();
+    dep_release();
     constexpr int VE = vec_elems<T>();
     constexpr int KM = 8 / CB;  // ranks this instantiation handles (k <= KM)
     const int nv = d / VE;
@@ -136,31 +140,22 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_
     if (p.rows_max == 0) return cudaSuccess;
     const unsigned g = grid_for(p.rows_max);
     if (p.dtype == MOE_BF16)
-        dispatch_kernel<__nv_bfloat16><<<g, kThreads, 0, s>>>(
-            p.T, p.rows_max, p.E, p.d, (const __nv_bfloat16*)x, row_token, expert_offsets,
-            (__nv_bfloat16*)xd);
-    else
-        dispatch_kernel<float><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, (const float*)x,
-                                                      row_token, expert_offsets, (float*)xd);
-    return cudaGetLastError();
+        return launch_k(dispatch_kernel<__nv_bfloat16>, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E,
+                        p.d, (const __nv_bfloat16*)x, row_token, expert_offsets, (__nv_bfloat16*)xd);
+    return launch_k(dispatch_kernel<float>, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d,
+                    (const float*)x, row_token, expert_offsets, (float*)xd);
 }
 
 template <typename T>
-void launch_combine_t(const Problem& p, unsigned g, const void* yd, const int32_t* topk_idx,
-                      const int32_t* slot_pos, const int32_t* expert_offsets, const float* topk_gate,
-                      const void* residual, void* y, cudaStream_t s) {
+cudaError_t launch_combine_t(const Problem& p, unsigned g, const void* yd, const int32_t* topk_idx,
+                             const int32_t* slot_pos, const int32_t* expert_offsets, const float* topk_gate,
+                             const void* residual, void* y, cudaStream_t s) {
     const T* ydt = (const T*)yd;
     const T* rt = (const T*)residual;
     T* yt = (T*)y;
-    if (p.k <= 2)
-        combine_kernel<T, 4><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx, slot_pos,
-                                                    expert_offsets, topk_gate, rt, yt);
-    else if (p.k <= 4)
-        combine_kernel<T, 2><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx, slot_pos,
-                                                    expert_offsets, topk_gate, rt, yt);
-    else
-        combine_kernel<T, 1><<<g, kThreads, 0, s>>>(p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx, slot_pos,
-                                                    expert_offsets, topk_gate, rt, yt);
+    auto kern = p.k <= 2 ? combine_kernel<T, 4> : p.k <= 4 ? combine_kernel<T, 2> : combine_kernel<T, 1>;
+    return launch_k(kern, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx,
+                    slot_pos, expert_offsets, topk_gate, rt, yt);
 }
 
 cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk_idx,
@@ -169,11 +164,9 @@ cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk
     if (p.T == 0) return cudaSuccess;
     const unsigned g = grid_for(p.T);
     if (p.dtype == MOE_BF16)
-        launch_combine_t<__nv_bfloat16>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y,
-                                        s);
-    else
-        launch_combine_t<float>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y, s);
-    return cudaGetLastError();
+        return launch_combine_t<__nv_bfloat16>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate,
+                                               residual, y, s);
+    return launch_combine_t<float>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y, s);
 }
 
 }  // namespace moe

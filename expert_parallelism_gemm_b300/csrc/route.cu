@@ -119,6 +119,8 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     const int nchunks = (d + kKC - 1) / kKC;
     const int nq = npass * nchunks;
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+    dep_wait();
+    dep_release();
 
     // copies of flattened chunk q = (pass, chunk) into ring slot q % S; always
     // commits a group
@@ -301,9 +303,8 @@ cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, cons
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
-    kern<<<grid, kRouteThreads, smem, s>>>(p.T, p.d, p.E, p.k, (const T*)x, (const T*)Wg, bias, topk_idx,
-                                          topk_gate, probs, scan);
-    return cudaGetLastError();
+    return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, p.T, p.d, p.E, p.k, (const T*)x,
+                    (const T*)Wg, bias, topk_idx, topk_gate, probs, scan);
 }
 
 }  // namespace
