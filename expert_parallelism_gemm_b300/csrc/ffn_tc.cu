@@ -14,20 +14,33 @@
 //            gate columns and the 128 matching up columns)
 //   down:    yd[r, :] = h[r] W2[e]^T
 // Ragged expert sizes stay on the device: each CTA reads expert_offsets,
-// counts the m-tiles of every expert and walks the tile list
-// (expert, n-tile, m-tile) persistently with stride gridDim.x, so the CTAs
-// running at one time share weight tiles through L2.
+// counts the m-tiles of every expert and walks the tile list persistently.
+//
+// CTAs run in clusters of two on neighbouring SMs and compute 256 x 256
+// tiles together with the 2-SM form of the tensor-core MMA
+// (tcgen05.mma.cta_group::2, M = 256): CTA rank r holds the 128 A rows of
+// m-tile 2*mp + r and one 128-row half of the 256-row weight tile, and each
+// CTA's tensor memory receives its own 128 accumulator rows.  Per k-step an SM
+// therefore takes in 32 KB of operands instead of the 48 KB a one-SM
+// 128 x 256 tile needs, which is what bounds this kernel, and six stages fit.
+// A cluster walks the list of pair tiles (expert, n-tile, m-tile pair) with
+// stride = number of clusters.  An m-tile with no rows (odd count) still takes
+// part in its pair's loads and MMAs and stores nothing.
 //
 // Per CTA (one per SM, 192 threads):
-//   warp 0   TMA producer: A tile [128 x 64] and B tile [256 x 64] per stage,
-//            128-byte swizzle, 4 stages of 48 KB;
-//   warp 1   TMEM allocation (512 columns = two 128 x 256 fp32
-//            accumulators) and, on one lane, the MMA issuer:
-//            tcgen05.mma.cta_group::1.kind::f16, M=128, N=256, K=16, bf16 in,
-//            fp32 accumulate, tcgen05.commit to free a stage / publish a tile;
-//   warps 2-5 epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
-//            lanes 32*(w%4)..+31 = the tile's rows), activation, bf16 round,
-//            masked stores of the rows that belong to the tile's expert.
+//   warp 0   TMA producer: its A tile [128 x 64] and its B half [128 x 64]
+//            per stage (128-byte swizzle, 6 stages of 32 KB); both CTAs'
+//            copies complete on the leader CTA's "full" barrier;
+//   warp 1   tensor-memory allocation (512 columns = two 128 x 256 fp32
+//            accumulators, allocated by both CTAs together) and, in the
+//            leader CTA on one lane, the MMA issuer: M=256, N=256, K=16, bf16
+//            in, fp32 accumulate; each commit arrives on the barriers of both
+//            CTAs (stage free / tile done);
+//   warps 2-5 epilogue: tcgen05.ld of this CTA's accumulator rows (warp w
+//            reads TMEM lanes 32*(w%4)..+31), activation, bf16 round, masked
+//            stores of the rows that belong to the tile's expert; then both
+//            CTAs' epilogue warps release the accumulator on the leader's
+//            barrier.
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // kDevTimeout in the status word, stops issuing work, waits (bounded) for its
 // own copies and MMAs in flight, frees its TMEM and returns.
@@ -42,13 +55,14 @@ constexpr int BM = 128;       // rows per tile (MMA M)
 constexpr int BN = 256;       // MMA N (gate/up: 128 + 128 columns)
 constexpr int BK = 64;        // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int UK = 16;        // K per MMA instruction
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int kTcThreads = 192;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES / 2;  // own A tile + own half of B
 constexpr int TMEM_COLS = 512;
 constexpr int kMaxE = 256;
+constexpr int kCluster = 2;   // CTAs per cluster (the pair of one 2-SM MMA)
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: far above any legitimate wait
 
 // shared-memory map after the 1024-aligned stage area
@@ -94,13 +108,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
         " selp.u32 %0, 1, 0, p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -134,13 +145,34 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, int* 
         }
     }
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
-                                            int c1) {
+// A tile into this CTA's shared memory, completing its bytes on `bar`, a
+// barrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                                 int c1) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
+}
+// shared::cluster address of the same shared variable in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs of the cluster meets here.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -160,17 +192,30 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
+// 2-SM MMA, issued by the leader CTA: A rows and B columns come half from
+// each CTA of the pair (same shared-memory offsets), D rows land in each CTA's
+// own tensor memory.
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Arrive on the barrier at offset `bar` of this CTA once the MMAs issued so
+// far complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+// The same, on the barrier at offset `bar` in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
 }
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -188,11 +233,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// Tile -> (expert, m-tile, n-tile).  tstart[e] = first tile of expert e; the
-// largest e with tstart[e] <= tile always has rows (empty experts share the
-// next expert's start).
-__device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int E, int n_tiles, int& e,
-                                            int& mt, int& nt) {
+// Pair tile -> (expert, m-tile of this CTA, n-tile).  tstart[e] = first pair
+// tile of expert e; the largest e with tstart[e] <= tile always has rows
+// (empty experts share the next expert's start).  An expert with mte m-tiles
+// has ceil(mte / 2) m-tile pairs; rank r of the cluster takes m-tile
+// 2 * pair + r.
+__device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int E, int n_tiles, int rank,
+                                            int& e, int& mt, int& nt) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -201,9 +248,9 @@ __device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int E, 
     }
     e = lo;
     const int local = tile - S.tstart[e];
-    const int mte = (S.offs[e + 1] - S.offs[e] + BM - 1) / BM;
-    nt = local / mte;
-    mt = local - nt * mte;
+    const int mpe = ((S.offs[e + 1] - S.offs[e] + BM - 1) / BM + 1) / 2;
+    nt = local / mpe;
+    mt = 2 * (local - nt * mpe) + rank;
 }
 
 template <bool SWIGLU>
@@ -216,26 +263,31 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     TcShared& S = *reinterpret_cast<TcShared*>(stages + (size_t)STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = args.E;
+    const int rank = (int)cluster_rank();
+    const int cluster = blockIdx.x / kCluster, nclusters = gridDim.x / kCluster;
+    constexpr uint16_t kPairMask = (1u << kCluster) - 1;
+    const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&S.full[s]), 1);
-            mbar_init(smem_u32(&S.empty[s]), 1);
+            mbar_init(smem_u32(&S.full[s]), 1);   // leader: its expect_tx; both CTAs' bytes
+            mbar_init(smem_u32(&S.empty[s]), 1);  // the leader's MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&S.tfull[b]), 1);
-            mbar_init(smem_u32(&S.tempty[b]), 4);
+            mbar_init(smem_u32(&S.tempty[b]), 4 * kCluster);  // leader: epilogue warps of both CTAs
         }
         mbar_init(smem_u32(&S.drain), 1);
         S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+        // one warp of each CTA of the pair allocates together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&S.tmem_base)),
                      "r"(TMEM_COLS)
                      : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     // global memory only from here on (earlier kernels on the stream are done)
     dep_wait();
@@ -253,7 +305,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int o0 = args.expert_offsets[e], o1 = args.expert_offsets[e + 1];
                 bad |= o0 < 0 || o1 < o0 || o1 > args.rows_max;
                 S.offs[e] = o0;
-                loc += (o1 - o0 + BM - 1) / BM * args.n_tiles;
+                loc += ((o1 - o0 + BM - 1) / BM + 1) / 2 * args.n_tiles;
             }
         }
         if (__any_sync(0xffffffffu, bad)) {
@@ -273,7 +325,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 S.tstart[e] = run;
                 if (loc > 0) {
                     const int o0 = args.expert_offsets[e], o1 = args.expert_offsets[e + 1];
-                    run += (o1 - o0 + BM - 1) / BM * args.n_tiles;
+                    run += ((o1 - o0 + BM - 1) / BM + 1) / 2 * args.n_tiles;
                 }
             }
         }
@@ -284,6 +336,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
+    // both CTAs' barriers are initialised before either signals the other
+    cluster_sync();
     tc_fence_after();
 
     const int total_tiles = S.tstart[E];
@@ -298,27 +352,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t phase = 0;
         int issued_parity[STAGES];
         for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-        for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
+        for (int tile = cluster; tile < total_tiles && !*abort_flag; tile += nclusters) {
             int e, mt, nt;
-            tile_coords(tile, S, E, n_tiles, e, mt, nt);
+            tile_coords(tile, S, E, n_tiles, rank, e, mt, nt);
             const int a_row = S.offs[e] + mt * BM;
-            const int b_row = e * args.wrows + nt * (SWIGLU ? BN / 2 : BN);
+            // this CTA's half of the weight tile: SwiGLU rank 0 the W1 (gate)
+            // rows, rank 1 the W3 (up) rows; down: rows 0-127 / 128-255
+            const int b_row = e * args.wrows + nt * (SWIGLU ? BN / 2 : BN) + (SWIGLU ? 0 : rank * (BN / 2));
+            const CUtensorMap* bmap = (SWIGLU && rank == 1) ? &tmB3 : &tmB;
             bool ok = true;
             for (int kb = 0; kb < k_blocks; ++kb) {
                 if (!wait_phase(smem_u32(&S.empty[stage]), phase ^ 1u, abort_flag, status)) {
                     ok = false;
                     break;
                 }
-                const uint32_t fb = smem_u32(&S.full[stage]);
                 const uint32_t sa = smem_u32(stages + (size_t)stage * STAGE_BYTES);
-                mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                tma_load_2d(sa, &tmA, fb, kb * BK, a_row);
-                if (SWIGLU) {
-                    tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, b_row);
-                    tma_load_2d(sa + A_BYTES + B_BYTES / 2, &tmB3, fb, kb * BK, b_row);
-                } else {
-                    tma_load_2d(sa + A_BYTES, &tmB, fb, kb * BK, b_row);
-                }
+                // the leader's full barrier counts both CTAs' bytes of the stage
+                const uint32_t fb = map_to_rank(smem_u32(&S.full[stage]), 0);
+                if (leader) mbar_arrive_expect_tx(smem_u32(&S.full[stage]), kCluster * STAGE_BYTES);
+                tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
+                tma_load_2d_pair(sa + A_BYTES, bmap, fb, kb * BK, b_row);
                 issued_parity[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -327,17 +380,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             if (!ok) break;
         }
-        // copies still in flight must land before the CTA leaves
+        // copies still in flight must land before the CTA leaves: the leader
+        // sees them on its full barriers; the other CTA once the leader's MMA
+        // has released the stage they filled
         for (int s = 0; s < STAGES; ++s)
-            if (issued_parity[s] >= 0) drain_phase(smem_u32(&S.full[s]), (uint32_t)issued_parity[s], status);
-    } else if (warp == 1 && lane == 0) {
+            if (issued_parity[s] >= 0)
+                drain_phase(smem_u32(leader ? &S.full[s] : &S.empty[s]), (uint32_t)issued_parity[s], status);
+    } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------- MMA issuer --
-        constexpr uint32_t idesc = idesc_bf16(BM, BN);
+        constexpr uint32_t idesc = idesc_bf16(kCluster * BM, BN);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int tile = cluster; tile < total_tiles; tile += nclusters) {
             if (!wait_phase(smem_u32(&S.tempty[acc]), acc_phase ^ 1u, abort_flag, status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -352,16 +408,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < BK / UK; ++kk)
-                    mma_bf16(d_tmem, sw128_desc(sa + kk * UK * 2), sw128_desc(sb + kk * UK * 2), idesc,
-                             (kb | kk) != 0);
-                mma_commit(smem_u32(&S.empty[stage]));
+                    mma_bf16_pair(d_tmem, sw128_desc(sa + kk * UK * 2), sw128_desc(sb + kk * UK * 2), idesc,
+                                  (kb | kk) != 0);
+                mma_commit_mc(smem_u32(&S.empty[stage]), kPairMask);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            mma_commit(smem_u32(&S.tfull[acc]));
+            mma_commit_mc(smem_u32(&S.tfull[acc]), kPairMask);
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -376,9 +432,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         uint32_t acc_phase = 0;
         __nv_bfloat16* out = args.out;
         const int n_out = args.n_out;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        for (int tile = cluster; tile < total_tiles; tile += nclusters) {
             int e, mt, nt;
-            tile_coords(tile, S, E, n_tiles, e, mt, nt);
+            tile_coords(tile, S, E, n_tiles, rank, e, mt, nt);
             if (!wait_phase(smem_u32(&S.tfull[acc]), acc_phase, abort_flag, status)) break;
             tc_fence_after();
             const int rows_e = S.offs[e + 1] - S.offs[e];
@@ -436,16 +492,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&S.tempty[acc]));
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&S.tempty[acc]), 0));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
     }
     tc_fence_before();
     __syncthreads();
+    // no CTA leaves (or frees tensor memory) while its peer may still read
+    // its operands, write its accumulators or arrive on its barriers
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS)
                      : "memory");
     }
@@ -494,6 +553,49 @@ int num_sms() {
     return n;
 }
 
+// Cluster launch (pairs of CTAs) with programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pairs(void (*kern)(KArgs...), unsigned clusters, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(clusters * kCluster);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Clusters of two that can be resident at once (one CTA per SM).
+int max_pairs() {
+    static int n = 0;
+    if (n == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(num_sms() / kCluster * kCluster));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true>, &cfg) != cudaSuccess || c <= 0)
+            c = num_sms() / kCluster;
+        n = c;
+    }
+    return n;
+}
+
 }  // namespace
 
 cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
@@ -506,7 +608,7 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
     const uint64_t rows = (uint64_t)p.rows_max, E = (uint64_t)p.E;
     if (!make_map(enc, &mA1, xd, rows, p.d, BM) || !make_map(enc, &mB1, W1, E * p.ffn, p.d, BN / 2) ||
         !make_map(enc, &mB3, W3, E * p.ffn, p.d, BN / 2) || !make_map(enc, &mA2, h, rows, p.ffn, BM) ||
-        !make_map(enc, &mB2, W2, E * p.d, p.ffn, BN))
+        !make_map(enc, &mB2, W2, E * p.d, p.ffn, BN / 2))
         return cudaErrorInvalidValue;
 
     static bool attr_done = false;
@@ -519,23 +621,24 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
         if (e2 != cudaSuccess) return e2;
         attr_done = true;
     }
-    // upper bound of m-tiles over all experts: sum_e ceil(n_e / BM) with
-    // sum_e n_e <= rows_max and n_e <= C
-    const int64_t mt_bound = std::min<int64_t>((int64_t)p.E * ceil_div(p.C, BM), ceil_div(p.rows_max, BM) + p.E);
-    const int sms = num_sms();
+    // upper bound of m-tile pairs over all experts: sum_e ceil(mt_e / 2) with
+    // mt_e = ceil(n_e / BM), n_e <= C, sum_e mt_e <= ceil(rows_max / BM) + E
+    const int64_t mp_bound = std::min<int64_t>((int64_t)p.E * ceil_div(ceil_div(p.C, BM), 2),
+                                               ceil_div(ceil_div(p.rows_max, BM) + 2 * (int64_t)p.E, 2));
+    const int pairs = max_pairs();
 
     TcArgs a1{p.E, (int)ceil_div(p.ffn, BN / 2), (int)ceil_div(p.d, BK), p.ffn, p.ffn, (int)p.rows_max,
               expert_offsets,
               (__nv_bfloat16*)h, status};
-    const unsigned g1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(sms, mt_bound * a1.n_tiles));
-    cudaError_t err = launch_k(tc_gemm_kernel<true>, dim3(g1), dim3(kTcThreads), kSmemBytes, s, mA1, mB1, mB3, a1);
+    const unsigned c1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(pairs, mp_bound * a1.n_tiles));
+    cudaError_t err = launch_pairs(tc_gemm_kernel<true>, c1, s, mA1, mB1, mB3, a1);
     if (err != cudaSuccess) return err;
 
     TcArgs a2{p.E, (int)ceil_div(p.d, BN), (int)ceil_div(p.ffn, BK), p.d, p.d, (int)p.rows_max,
               expert_offsets,
               (__nv_bfloat16*)yd, status};
-    const unsigned g2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(sms, mt_bound * a2.n_tiles));
-    return launch_k(tc_gemm_kernel<false>, dim3(g2), dim3(kTcThreads), kSmemBytes, s, mA2, mB2, mB2, a2);
+    const unsigned c2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(pairs, mp_bound * a2.n_tiles));
+    return launch_pairs(tc_gemm_kernel<false>, c2, s, mA2, mB2, mB2, a2);
 }
 
 }  // namespace moe
