@@ -41,7 +41,7 @@ class moe_problem(ctypes.Structure):
 
 _LAYOUT_FIELDS = ("status", "topk_idx", "topk_gate", "slot_pos", "counts_routed", "counts_kept",
                   "expert_offsets", "shard_offsets", "shard_routed", "shard_overflow", "dropped",
-                  "hist", "row_token", "xd", "h", "yd", "total")
+                  "hist", "row_token", "xd", "h", "yd", "ffn_sync", "total")
 
 
 class moe_workspace_layout(ctypes.Structure):

@@ -86,6 +86,7 @@ void layout(const Problem& p, moe_workspace_layout* L) {
     L->xd = take(rm * p.d * eb);
     L->h = take(rm * p.ffn * eb);
     L->yd = take(rm * p.d * eb);
+    L->ffn_sync = take(ffn_sync_ints(p) * sizeof(int32_t));
     L->total = o;
 }
 
@@ -189,7 +190,8 @@ int moe_expert_ffn(const moe_problem* mp, const void* xd, const int32_t* expert_
     int* status = (int*)((char*)ws + L.status);
     cudaStream_t s = (cudaStream_t)stream;
     if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
-        cudaError_t e = launch_ffn_tc(p, xd, expert_offsets, W1, W3, W2, h, yd, status, s);
+        cudaError_t e = launch_ffn_tc(p, xd, expert_offsets, W1, W3, W2, h, yd, status,
+                                      (int*)((char*)ws + L.ffn_sync), s);
         if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
         return cuda_rc(e);
     }
@@ -245,7 +247,7 @@ int moe_layer_forward(const moe_problem* mp, const void* x, const void* Wg, cons
     if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
     if (e == cudaSuccess) {
         if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
-            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, s);
+            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, (int*)(w + L.ffn_sync), s);
             if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
         } else {
             e = launch_ffn_simt(p, xd, off, W1, W3, W2, h, yd, s);

@@ -163,8 +163,11 @@ cudaError_t launch_ffn_simt(const Problem& p, const void* xd, const int32_t* exp
 
 // tcgen05 grouped GEMM path (bf16 + SwiGLU). Returns cudaErrorNotSupported
 // when the tensor-map encoder cannot be obtained.
+// `sync` is the workspace's ffn_sync region (ffn_sync_ints(p) ints, zero
+// before the first launch; each launch leaves it zero again).
 cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
                           const void* W1, const void* W3, const void* W2, void* h, void* yd,
-                          int* status, cudaStream_t s);
+                          int* status, int* sync, cudaStream_t s);
+size_t ffn_sync_ints(const Problem& p);
 
 }  // namespace moe

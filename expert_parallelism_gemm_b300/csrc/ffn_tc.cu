@@ -8,11 +8,19 @@
 // Bottleneck" (ashishsrivastav.com), phase 3: each device multiplies only the
 // tokens assigned to its local experts.
 //
-// Two launches over the packed, expert-major rows:
+// One persistent launch over the packed, expert-major rows computes both
 //   gate/up: h[r, :] = silu(xd[r] W1[e]^T) * (xd[r] W3[e]^T)   (SwiGLU fused
 //            into the epilogue: one 128 x 256 accumulator tile holds 128
 //            gate columns and the 128 matching up columns)
 //   down:    yd[r, :] = h[r] W2[e]^T
+// from one tile list: each expert's gate/up tiles, then -- once `lag` more
+// tiles (two waves of clusters) have been placed -- its down tiles.  A down
+// tile reads h rows of one (expert, m-tile pair); its producer waits (bounded,
+// acquire) until the four epilogue warps of both CTAs of every gate/up tile
+// of that pair have stored their rows and released a counter, then issues its
+// TMA loads after a proxy fence.  With the slack the wait is rarely taken, and
+// there is no tail between the two GEMMs.  The last CTA to leave zeroes the
+// counters for the next launch.
 // Ragged expert sizes stay on the device: each CTA reads expert_offsets,
 // counts the m-tiles of every expert and walks the tile list persistently.
 //
@@ -74,21 +82,30 @@ struct __align__(8) TcShared {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int nseg;
+    int total_tiles;
     int offs[kMaxE + 1];
-    int tstart[kMaxE + 1];
+    int seg_start[2 * kMaxE + 1];  // first tile of each segment, then the total
+    int seg_info[2 * kMaxE];       // kind << 16 | expert (kind 0 gate/up, 1 down)
+    int queue[kMaxE];              // experts whose down segments are not placed yet
+    int queue_end[kMaxE];          // tile position where each one's gate/up segment ends
 };
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(TcShared);
 
-struct TcArgs {
-    int E;
-    int n_tiles;     // n-tiles per expert
-    int k_blocks;    // ceil(K / BK)
-    int n_out;       // output columns (ffn for gate/up, d for down)
-    int wrows;       // weight rows per expert in the flattened [E * wrows, K] map
-    int rows_max;    // rows of the packed A / output buffers
+struct FfnArgs {
+    int E, d, ffn, rows_max;
+    int n1, k1;    // gate/up: n-tiles of 128 output columns per expert, k-blocks over d
+    int n2, k2;    // down: n-tiles of 256 output columns per expert, k-blocks over ffn
+    int mp_cap;    // bound on m-tile pairs per expert
+    int lag;       // tiles placed between an expert's last gate/up tile and its down tiles
     const int32_t* expert_offsets;
-    __nv_bfloat16* out;
+    __nv_bfloat16* h;
+    __nv_bfloat16* yd;
     int* status;
+    // [0] exit ticket; [1 + e * mp_cap + mp] epilogue-warp releases of the
+    // gate/up pair tiles of (expert e, m-pair mp).  Zero at launch; the last
+    // CTA to leave zeroes it again.
+    int* sync;
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -233,30 +250,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// Pair tile -> (expert, m-tile of this CTA, n-tile).  tstart[e] = first pair
-// tile of expert e; the largest e with tstart[e] <= tile always has rows
-// (empty experts share the next expert's start).  An expert with mte m-tiles
-// has ceil(mte / 2) m-tile pairs; rank r of the cluster takes m-tile
-// 2 * pair + r.
-__device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int E, int n_tiles, int rank,
-                                            int& e, int& mt, int& nt) {
-    int lo = 0, hi = E - 1;
+// Tile -> (kind, expert, m-tile of this CTA, n-tile, m-pair).  Segment s
+// covers the tiles [seg_start[s], seg_start[s+1]) of one kind and expert, in
+// (n-tile, m-pair) order with the m-pair fastest, so consecutive tiles share
+// the weight tile.  An expert with mte m-tiles has ceil(mte / 2) m-tile
+// pairs; rank r of the cluster takes m-tile 2 * pair + r.
+__device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int n1, int n2, int rank, int& kind,
+                                            int& e, int& mt, int& nt, int& mp) {
+    int lo = 0, hi = S.nseg - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (S.tstart[mid] <= tile) lo = mid;
+        if (S.seg_start[mid] <= tile) lo = mid;
         else hi = mid - 1;
     }
-    e = lo;
-    const int local = tile - S.tstart[e];
+    kind = S.seg_info[lo] >> 16;
+    e = S.seg_info[lo] & 0xffff;
+    const int local = tile - S.seg_start[lo];
     const int mpe = ((S.offs[e + 1] - S.offs[e] + BM - 1) / BM + 1) / 2;
+    (void)n1;
+    (void)n2;
     nt = local / mpe;
-    mt = 2 * (local - nt * mpe) + rank;
+    mp = local - nt * mpe;
+    mt = 2 * mp + rank;
 }
 
-template <bool SWIGLU>
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
-tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-               const __grid_constant__ CUtensorMap tmB3, const TcArgs args) {
+tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+              const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmA2,
+              const __grid_constant__ CUtensorMap tmB2, const FfnArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* stages = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -293,45 +320,42 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     dep_wait();
     dep_release();
     if (warp == 0) {
-        // expert offsets and per-expert tile starts (warp-wide scan)
-        // offsets must be non-decreasing within [0, rows_max]; otherwise the
-        // kernel records kDevBadIndex and computes nothing
-        const int per = (E + 31) / 32;
-        int loc = 0;
+        // expert offsets; they must be non-decreasing within [0, rows_max],
+        // otherwise the kernel records kDevBadIndex and computes nothing
         bool bad = false;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) {
-                const int o0 = args.expert_offsets[e], o1 = args.expert_offsets[e + 1];
-                bad |= o0 < 0 || o1 < o0 || o1 > args.rows_max;
-                S.offs[e] = o0;
-                loc += ((o1 - o0 + BM - 1) / BM + 1) / 2 * args.n_tiles;
+        for (int e = lane; e <= E; e += 32) {
+            const int o = args.expert_offsets[e];
+            S.offs[e] = o;
+            bad |= o < 0 || o > args.rows_max || (e > 0 && o < args.expert_offsets[e - 1]);
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        __syncwarp();
+        if (lane == 0) {
+            if (bad && blockIdx.x == 0) atomicOr(args.status, kDevBadIndex);
+            // tile list: gate/up segments in expert order; an expert's down
+            // segment follows once `lag` further tiles have been placed after
+            // its gate/up segment (or at the end)
+            int pos = 0, nseg = 0, qh = 0, qt = 0;
+            auto pairs = [&](int e) { return ((S.offs[e + 1] - S.offs[e] + BM - 1) / BM + 1) / 2; };
+            auto place_down = [&](int e) {
+                S.seg_start[nseg] = pos;
+                S.seg_info[nseg++] = (1 << 16) | e;
+                pos += pairs(e) * args.n2;
+            };
+            for (int e = 0; e < E && !bad; ++e) {
+                const int mpe = pairs(e);
+                if (mpe == 0) continue;
+                S.seg_start[nseg] = pos;
+                S.seg_info[nseg++] = e;
+                pos += mpe * args.n1;
+                S.queue[qt] = e;
+                S.queue_end[qt++] = pos;
+                while (qh < qt && pos - S.queue_end[qh] >= args.lag) place_down(S.queue[qh++]);
             }
-        }
-        if (__any_sync(0xffffffffu, bad)) {
-            loc = 0;
-            if (lane == 0 && blockIdx.x == 0) atomicOr(args.status, kDevBadIndex);
-        }
-        int incl = loc;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
-        }
-        int run = incl - loc;
-        for (int j = 0; j < per; ++j) {
-            const int e = lane * per + j;
-            if (e < E) {
-                S.tstart[e] = run;
-                if (loc > 0) {
-                    const int o0 = args.expert_offsets[e], o1 = args.expert_offsets[e + 1];
-                    run += ((o1 - o0 + BM - 1) / BM + 1) / 2 * args.n_tiles;
-                }
-            }
-        }
-        if (lane == 31) {
-            S.tstart[E] = incl;
-            S.offs[E] = args.expert_offsets[E];
+            while (qh < qt) place_down(S.queue[qh++]);
+            S.seg_start[nseg] = pos;
+            S.nseg = nseg;
+            S.total_tiles = pos;
         }
     }
     tc_fence_before();
@@ -340,11 +364,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     cluster_sync();
     tc_fence_after();
 
-    const int total_tiles = S.tstart[E];
+    const int total_tiles = S.total_tiles;
     const uint32_t tmem_base = S.tmem_base;
     volatile int* abort_flag = &S.abort_flag;
     int* status = args.status;
-    const int n_tiles = args.n_tiles, k_blocks = args.k_blocks;
+    const int n1 = args.n1, n2 = args.n2;
 
     if (warp == 0 && lane == 0) {
         // ------------------------------------------------ TMA producer --
@@ -353,13 +377,44 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int issued_parity[STAGES];
         for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
         for (int tile = cluster; tile < total_tiles && !*abort_flag; tile += nclusters) {
-            int e, mt, nt;
-            tile_coords(tile, S, E, n_tiles, rank, e, mt, nt);
+            int kind, e, mt, nt, mp;
+            tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
             const int a_row = S.offs[e] + mt * BM;
-            // this CTA's half of the weight tile: SwiGLU rank 0 the W1 (gate)
-            // rows, rank 1 the W3 (up) rows; down: rows 0-127 / 128-255
-            const int b_row = e * args.wrows + nt * (SWIGLU ? BN / 2 : BN) + (SWIGLU ? 0 : rank * (BN / 2));
-            const CUtensorMap* bmap = (SWIGLU && rank == 1) ? &tmB3 : &tmB;
+            const CUtensorMap* amap;
+            const CUtensorMap* bmap;
+            int b_row, k_blocks;
+            if (kind == 0) {
+                // gate/up: rank 0 loads the W1 (gate) rows, rank 1 the W3 (up) rows
+                amap = &tmA1;
+                bmap = rank == 1 ? &tmB3 : &tmB1;
+                b_row = e * args.ffn + nt * (BN / 2);
+                k_blocks = args.k1;
+            } else {
+                // down: rank r loads rows 128 r .. 128 r + 127 of the 256-row W2 tile
+                amap = &tmA2;
+                bmap = &tmB2;
+                b_row = e * args.d + nt * BN + rank * (BN / 2);
+                k_blocks = args.k2;
+                // its A rows are h rows of (e, mp): wait until every gate/up pair
+                // tile of them has been stored (four epilogue warps in each CTA)
+                const int* cnt = args.sync + 1 + (size_t)e * args.mp_cap + mp;
+                const int target = 4 * kCluster * n1;
+                if (ld_acquire(cnt) < target) {
+                    const uint64_t t0 = globaltimer();
+                    while (ld_acquire(cnt) < target) {
+                        if (*abort_flag) break;
+                        if (globaltimer() - t0 > kTimeoutNs) {
+                            *abort_flag = 1;
+                            atomicOr(status, kDevTimeout);
+                            break;
+                        }
+                    }
+                }
+                if (*abort_flag) break;
+                // the stores were made through the generic proxy; TMA reads
+                // through the async proxy
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
             bool ok = true;
             for (int kb = 0; kb < k_blocks; ++kb) {
                 if (!wait_phase(smem_u32(&S.empty[stage]), phase ^ 1u, abort_flag, status)) {
@@ -370,7 +425,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // the leader's full barrier counts both CTAs' bytes of the stage
                 const uint32_t fb = map_to_rank(smem_u32(&S.full[stage]), 0);
                 if (leader) mbar_arrive_expect_tx(smem_u32(&S.full[stage]), kCluster * STAGE_BYTES);
-                tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
+                tma_load_2d_pair(sa, amap, fb, kb * BK, a_row);
                 tma_load_2d_pair(sa + A_BYTES, bmap, fb, kb * BK, b_row);
                 issued_parity[stage] = (int)phase;
                 if (++stage == STAGES) {
@@ -394,6 +449,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = cluster; tile < total_tiles; tile += nclusters) {
+            int kind, e, mt, nt, mp;
+            tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
+            const int k_blocks = kind == 0 ? args.k1 : args.k2;
             if (!wait_phase(smem_u32(&S.tempty[acc]), acc_phase ^ 1u, abort_flag, status)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -430,20 +488,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int row_in_tile = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        __nv_bfloat16* out = args.out;
-        const int n_out = args.n_out;
         for (int tile = cluster; tile < total_tiles; tile += nclusters) {
-            int e, mt, nt;
-            tile_coords(tile, S, E, n_tiles, rank, e, mt, nt);
+            int kind, e, mt, nt, mp;
+            tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
             if (!wait_phase(smem_u32(&S.tfull[acc]), acc_phase, abort_flag, status)) break;
             tc_fence_after();
             const int rows_e = S.offs[e + 1] - S.offs[e];
             const int local_row = mt * BM + row_in_tile;
             const bool valid = local_row < rows_e;
-            __nv_bfloat16* orow = out + (size_t)(S.offs[e] + local_row) * n_out;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (SWIGLU) {
-                const int col0 = nt * (BN / 2);
+            if (kind == 0) {
+                // SwiGLU: columns 0-127 of the accumulator are gate, 128-255 up
+                const int n_out = args.ffn, col0 = nt * (BN / 2);
+                __nv_bfloat16* orow = args.h + (size_t)(S.offs[e] + local_row) * n_out;
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 16) {
                     uint32_t g[16], u[16];
@@ -471,7 +528,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
             } else {
-                const int col0 = nt * BN;
+                const int n_out = args.d, col0 = nt * BN;
+                __nv_bfloat16* orow = args.yd + (size_t)(S.offs[e] + local_row) * n_out;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 16) {
                     uint32_t a[16];
@@ -493,6 +551,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&S.tempty[acc]), 0));
+            if (kind == 0) {
+                // release this warp's h rows to the down tiles that read them
+                __threadfence();
+                __syncwarp();
+                if (lane == 0)
+                    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(
+                                     args.sync + 1 + (size_t)e * args.mp_cap + mp),
+                                 "r"(1)
+                                 : "memory");
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -507,6 +575,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                      "r"(TMEM_COLS)
                      : "memory");
+    }
+    // the last CTA out zeroes the release counters for the next launch
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(args.sync, 1) == (int)gridDim.x - 1) {
+            __threadfence();
+            const int n = 1 + E * args.mp_cap;
+            for (int i = 1; i < n; ++i) args.sync[i] = 0;
+            __threadfence();
+            args.sync[0] = 0;
+        }
     }
 }
 
@@ -589,7 +668,7 @@ int max_pairs() {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, tc_gemm_kernel<true>, &cfg) != cudaSuccess || c <= 0)
+        if (cudaOccupancyMaxActiveClusters(&c, tc_ffn_kernel, &cfg) != cudaSuccess || c <= 0)
             c = num_sms() / kCluster;
         n = c;
     }
@@ -598,9 +677,13 @@ int max_pairs() {
 
 }  // namespace
 
+size_t ffn_sync_ints(const Problem& p) {
+    return 1 + (size_t)p.E * (size_t)ceil_div(ceil_div(p.C, BM), 2);
+}
+
 cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
                           const void* W1, const void* W3, const void* W2, void* h, void* yd,
-                          int* status, cudaStream_t s) {
+                          int* status, int* sync, cudaStream_t s) {
     if (p.rows_max == 0) return cudaSuccess;
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cudaErrorNotSupported;
@@ -613,32 +696,41 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
 
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e1 = cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemBytes);
-        cudaError_t e2 = cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kSmemBytes);
+        cudaError_t e1 =
+            cudaFuncSetAttribute(tc_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e1 != cudaSuccess) return e1;
-        if (e2 != cudaSuccess) return e2;
         attr_done = true;
     }
     // upper bound of m-tile pairs over all experts: sum_e ceil(mt_e / 2) with
     // mt_e = ceil(n_e / BM), n_e <= C, sum_e mt_e <= ceil(rows_max / BM) + E
-    const int64_t mp_bound = std::min<int64_t>((int64_t)p.E * ceil_div(ceil_div(p.C, BM), 2),
-                                               ceil_div(ceil_div(p.rows_max, BM) + 2 * (int64_t)p.E, 2));
-    const int pairs = max_pairs();
-
-    TcArgs a1{p.E, (int)ceil_div(p.ffn, BN / 2), (int)ceil_div(p.d, BK), p.ffn, p.ffn, (int)p.rows_max,
-              expert_offsets,
-              (__nv_bfloat16*)h, status};
-    const unsigned c1 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(pairs, mp_bound * a1.n_tiles));
-    cudaError_t err = launch_pairs(tc_gemm_kernel<true>, c1, s, mA1, mB1, mB3, a1);
-    if (err != cudaSuccess) return err;
-
-    TcArgs a2{p.E, (int)ceil_div(p.d, BN), (int)ceil_div(p.ffn, BK), p.d, p.d, (int)p.rows_max,
-              expert_offsets,
-              (__nv_bfloat16*)yd, status};
-    const unsigned c2 = (unsigned)std::max<int64_t>(1, std::min<int64_t>(pairs, mp_bound * a2.n_tiles));
-    return launch_pairs(tc_gemm_kernel<false>, c2, s, mA2, mB2, mB2, a2);
+    const int64_t mp_cap = ceil_div(ceil_div(p.C, BM), 2);
+    const int64_t mp_bound =
+        std::min<int64_t>((int64_t)p.E * mp_cap, ceil_div(ceil_div(p.rows_max, BM) + 2 * (int64_t)p.E, 2));
+    FfnArgs a{};
+    a.E = p.E;
+    a.d = p.d;
+    a.ffn = p.ffn;
+    a.rows_max = (int)p.rows_max;
+    a.n1 = (int)ceil_div(p.ffn, BN / 2);
+    a.k1 = (int)ceil_div(p.d, BK);
+    a.n2 = (int)ceil_div(p.d, BN);
+    a.k2 = (int)ceil_div(p.ffn, BK);
+    a.mp_cap = (int)mp_cap;
+    a.expert_offsets = expert_offsets;
+    a.h = (__nv_bfloat16*)h;
+    a.yd = (__nv_bfloat16*)yd;
+    a.status = status;
+    a.sync = sync;
+    // Down tiles are several times longer than gate/up tiles (K = ffn vs d), so
+    // they all go after the last gate/up tile: every cluster then ends on one
+    // or two of them instead of a few clusters finishing the last expert's.
+    const int lag_tiles = 1 << 30;
+    // all clusters must be resident at once (down tiles wait on gate/up tiles
+    // of other clusters), so never more than the occupancy allows
+    const unsigned clusters =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_pairs(), mp_bound * (a.n1 + a.n2)));
+    a.lag = lag_tiles;
+    return launch_pairs(tc_ffn_kernel, clusters, s, mA1, mB1, mB3, mA2, mB2, a);
 }
 
 }  // namespace moe

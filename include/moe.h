@@ -100,6 +100,9 @@ typedef struct {
     size_t xd;             /* dtype[rows_max * d]: packed expert inputs      */
     size_t h;              /* dtype[rows_max * ffn]: expert hidden rows      */
     size_t yd;             /* dtype[rows_max * d]: packed expert outputs     */
+    size_t ffn_sync;       /* int32 scratch of the expert FFN (gate/up ->
+                              down release counters); every call leaves it
+                              zero again                                    */
     size_t total;          /* = moe_workspace_size                           */
 } moe_workspace_layout;
 

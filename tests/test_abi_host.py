@@ -99,7 +99,8 @@ def test_workspace_layout_is_aligned_and_disjoint():
                      counts_routed=4 * wl.E, counts_kept=4 * wl.E, expert_offsets=4 * (wl.E + 1),
                      shard_offsets=4 * (wl.D + 1), shard_routed=4 * wl.D, shard_overflow=4 * wl.D,
                      dropped=4, hist=4 * wl.E * wl.k * nblk, row_token=4 * rows_max,
-                     xd=eb * rows_max * wl.d, h=eb * rows_max * wl.ffn, yd=eb * rows_max * wl.d)
+                     xd=eb * rows_max * wl.d, h=eb * rows_max * wl.ffn, yd=eb * rows_max * wl.d,
+                     ffn_sync=4 * (1 + wl.E * -(-(-(-C // 128)) // 2)))
         spans = sorted((L[n], L[n] + s) for n, s in sizes.items())
         assert spans[0][0] == 0 == L["status"]
         for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
