@@ -45,11 +45,11 @@ import moe_inputs  # noqa: E402
 
 DEFAULT_WORKLOAD = "mixtral_scaled"
 METRIC = "MoE layer forward tokens/sec on 1 B300; % of HBM BW / BF16 tensor peak"
-# dram bytes (read + write) of one expert-FFN call (its two GEMM launches) on
-# the default workload, from the ncu capture summarised in
-# profiles/tc_gemm_mixtral_scaled_full.md; None whenever the kernels have
+# dram bytes (read + write) of one expert-FFN call on the default workload,
+# from the ncu capture of the current kernel summarised in
+# profiles/tc_ffn_mixtral_scaled_full.md; None whenever the kernel has
 # changed since that capture
-FFN_DRAM_BYTES = (134.328064 + 33.003520 + 119.070464 + 3.374336) * 1e6
+FFN_DRAM_BYTES = (250.475008 + 63.098368) * 1e6
 
 
 def _peaks():
@@ -307,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
                        "ffn": wl.ffn, "capacity_factor": wl.capacity_factor, "act": wl.act,
                        "C_expert": C, "kept": kept, "dropped": n_dropped,
                        "parallelism": f"replicas x{world}", "l2": "flushed before every step (2 x L2 write)"},
-            "roofline": {"kernel": "moe_expert_ffn (tcgen05 gate/up + down GEMMs)", "bound": "tensor",
+            "roofline": {"kernel": "moe_expert_ffn (one 2-SM tcgen05 launch: gate/up + down)", "bound": "tensor",
                          "achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
                          "frac": achieved_tf / bf16_tf,
                          "traffic": FFN_DRAM_BYTES if args.workload == DEFAULT_WORKLOAD else None,
@@ -325,8 +325,10 @@ def run_ours(args, rank, world, local_rank):
 
 def launches_per_step(wl) -> int:
     """Kernels of one moe_layer_forward: router with the fused count pass,
-    rank pass, dispatch, two FFN kernels, combine."""
-    return 1 + 1 + 1 + 2 + 1
+    rank pass, dispatch, expert FFN (one launch for the tensor-core path,
+    two for the SIMT path), combine."""
+    tc = wl.dtype == "bf16" and wl.act == "swiglu"
+    return 1 + 1 + 1 + (1 if tc else 2) + 1
 
 
 # -------------------------------------------------------------- oracle --
