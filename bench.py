@@ -116,6 +116,29 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# --------------------------------------------------------- multi-rank --
+def replica_workload(wl, rank: int):
+    """Each rank runs an independent layer instance (replicas): same shapes,
+    inputs drawn with a rank-specific seed."""
+    return wl.with_(seed=wl.seed + 1000 * rank)
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (all ranks get it); the identity on one rank."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_total_ms * 1e-3)
+
+
 # ------------------------------------------------------------ our path --
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -125,7 +148,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     wl = moe_inputs.WORKLOADS[args.workload]
-    inp = moe_inputs.make_inputs(wl.with_(seed=wl.seed + 1000 * rank), device=dev)
+    inp = moe_inputs.make_inputs(replica_workload(wl, rank), device=dev)
     p = moe.problem_of(wl)
     C, C_shard, rows_max = moe.moe_capacity(p)
     ws = moe.alloc_workspace(p, dev)
@@ -168,11 +191,7 @@ def run_ours(args, rank, world, local_rank):
             ends[i].record(stream)
         barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms_max = float(t.item())
+    total_ms_max = max_over_ranks(sum(step_ms), world, dev)
     status = moe.moe_device_status(ws, stream)
     if status != moe.MOE_OK:
         raise RuntimeError(f"device status after timed steps: {moe.moe_status_string(status)}")
@@ -255,11 +274,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
         e_e[i].record(stream)
     barrier()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e_s, e_e))
-    t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_ms_max = float(t.item())
+    e2e_ms_max = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)), world, dev)
 
     out = None
     if rank == 0:
@@ -288,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
             "combine": {"ms": per_call["combine"], "GB_s": gb(combine_bytes, per_call["combine"]),
                         "frac_hbm": gb(combine_bytes, per_call["combine"]) / hbm_gbs},
         }
-        value = world * wl.T * args.steps / (total_ms_max * 1e-3)
+        value = job_tokens_per_s(wl.T, world, args.steps, total_ms_max)
         clocks = clk.summary()
         out = {
             "metric": METRIC,
@@ -314,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
                          "peak_source": f"{peak_src} bf16 burst",
                          "algorithmic": f"2*3*d*ffn flops per kept row x {kept} rows"},
             "kernels": kernels,
-            "e2e": {"value": world * wl.T * args.steps / (e2e_ms_max * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_tokens_per_s(wl.T, world, args.steps, e2e_ms_max), "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * eb,
                     "api": "moe_layer_forward, pinned host x -> device -> host y"},
             "gpu_launches": args.steps * launches_per_step(wl),
