@@ -64,6 +64,7 @@ def _load():
         lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
         lib.oracle_combine.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, P]
         lib.oracle_token_outputs.argtypes = [i64, P, i32, i32, i32, i32, i32] + [P] * 9
+        lib.oracle_routing_stats.argtypes = [i64, i32, i32, P, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -191,6 +192,19 @@ def combine(yd: np.ndarray, topk_idx, slot_pos, topk_gate, expert_offsets,
     _load().oracle_combine(T, d, k, dtype, _ptr(idx), _ptr(sp), _ptr(gt), _ptr(eo), _ptr(ydd),
                            _ptr(ra), _ptr(y))
     return y
+
+
+def routing_stats(probs, counts_routed, counts_kept, k: int):
+    """Routing statistics in double: (aux, entropy, drop_fraction,
+    load_imbalance), and the per-expert mean router probability."""
+    pa = np.ascontiguousarray(probs, dtype=np.float32)
+    T, E = pa.shape
+    cr = np.ascontiguousarray(counts_routed, dtype=np.int32)
+    ck = np.ascontiguousarray(counts_kept, dtype=np.int32)
+    out = np.zeros(4, dtype=np.float64)
+    mp = np.zeros(E, dtype=np.float64)
+    _load().oracle_routing_stats(T, E, k, _ptr(pa), _ptr(cr), _ptr(ck), _ptr(out), _ptr(mp))
+    return out, mp
 
 
 def token_outputs(tokens, x, topk_idx, slot_pos, topk_gate, W1, W3, W2, act: int,

@@ -368,3 +368,54 @@ void oracle_token_outputs(int64_t n, const int64_t* tokens, int d, int f, int k,
         free(ye);
     }
 }
+
+/* ------------------------------------------------------------------------ *
+ * Routing statistics.  [NG] "Components and Architecture" and formal
+ * algorithm: the auxiliary load-balancing term is the sum over experts of
+ * the fraction of tokens sent to the expert times the fraction of router
+ * probability it receives; [IS] glossary: the load-balancing loss;
+ * "Expert Parallelism" intro page (nhimg.org), practitioner guidance: watch
+ * expert utilisation and routing entropy.
+ *
+ * Readings (the pages give the product form, not the normalisation):
+ *   f_e   = routed_e / (T*k), the share of the T*k pre-drop assignments;
+ *   P_e   = (1/T) sum_t p[t,e], the mean router probability;
+ *   aux   = E * sum_e f_e * P_e (the Switch scaling: 1 for perfectly uniform
+ *           routing, E when every token sends everything to one expert);
+ *   H     = (1/T) sum_t -sum_e p[t,e] ln p[t,e], with 0 ln 0 = 0 (nats);
+ *   drop  = (sum_e routed_e - kept_e) / (T*k);
+ *   imbal = max_e routed_e / (T*k/E), the hottest expert's load over the mean.
+ * All sums in double; out = {aux, H, drop, imbal}, mean_prob = P (may be
+ * NULL).  T = 0 gives zeros.
+ * ------------------------------------------------------------------------ */
+void oracle_routing_stats(int64_t T, int E, int k, const float* probs /* [T, E] */,
+                          const int32_t* counts_routed, const int32_t* counts_kept,
+                          double* out /* [4] */, double* mean_prob /* [E] or NULL */) {
+    double* P = (double*)calloc((size_t)E, sizeof(double));
+    double H = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        double ht = 0.0;
+        for (int e = 0; e < E; ++e) {
+            const double p = (double)probs[(size_t)t * E + e];
+            P[e] += p;
+            if (p > 0.0) ht -= p * log(p);
+        }
+        H += ht;
+    }
+    double aux = 0.0, routed = 0.0, kept = 0.0, maxr = 0.0;
+    const double Tk = (double)T * (double)k;
+    for (int e = 0; e < E; ++e) {
+        if (T > 0) P[e] /= (double)T;
+        const double f = Tk > 0.0 ? (double)counts_routed[e] / Tk : 0.0;
+        aux += f * P[e];
+        routed += counts_routed[e];
+        kept += counts_kept[e];
+        if (counts_routed[e] > maxr) maxr = counts_routed[e];
+        if (mean_prob) mean_prob[e] = P[e];
+    }
+    out[0] = (double)E * aux;
+    out[1] = T > 0 ? H / (double)T : 0.0;
+    out[2] = Tk > 0.0 ? (routed - kept) / Tk : 0.0;
+    out[3] = Tk > 0.0 ? maxr / (Tk / (double)E) : 0.0;
+    free(P);
+}

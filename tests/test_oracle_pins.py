@@ -445,3 +445,61 @@ def test_combine_converted_inputs_stay_alive():
         np.testing.assert_allclose(got, oracle.combine(yd64.astype(np.float32).astype(np.float64), idx,
                                                        s.slot_pos, gate, s.expert_offsets), rtol=0, atol=0)
     np.testing.assert_allclose(want, got, rtol=1e-6, atol=1e-6)
+
+
+# --------------------------------------------------------------------------
+# routing statistics (load-balancing term, entropy, drops, imbalance)
+# --------------------------------------------------------------------------
+def test_routing_stats_worked_example_closed_form():
+    # The [TI] worked example (6 tokens, 8 experts, top-2): every token has
+    # logit 3 at its rank-0 expert, 2 at its rank-1 expert, 0 elsewhere, so
+    # p = (e^3, e^2, 1 x 6) / S with S = e^3 + e^2 + 6.  Per expert, the mean
+    # probability times 6 is (#rank-0) e^3/S + (#rank-1) e^2/S + (#other)/S;
+    # with the routed counts (0, 3, 3, 2, 2, 1, 1, 0) over 12 assignments the
+    # load-balancing term E * sum f_e P_e works out by hand to
+    # (16 e^3 + 12 e^2 + 44) / (9 S).
+    rows = read_golden("worked_example.txt")
+    choices = [tuple(int(v) for v in r[2:4]) for r in rows if r[0] == "choice"]
+    assert len(choices) == 6
+    E, k = 8, 2
+    g = np.zeros((6, E), np.float32)
+    for t, (a, b) in enumerate(choices):
+        g[t, a], g[t, b] = 3.0, 2.0
+    probs, idx, _ = oracle.softmax_topk(g, k)
+    s = oracle.assign(idx, E, 4, 1.0)
+    out, mp = oracle.routing_stats(probs, s.counts_routed, s.counts_kept, k)
+    e3, e2 = math.exp(3.0), math.exp(2.0)
+    S = e3 + e2 + 6.0
+    assert out[0] == pytest.approx((16 * e3 + 12 * e2 + 44) / (9 * S), rel=1e-6)
+    a, b, c = e3 / S, e2 / S, 1.0 / S
+    assert out[1] == pytest.approx(-(a * math.log(a) + b * math.log(b) + 6 * c * math.log(c)), rel=1e-6)
+    assert out[2] == pytest.approx(2 / 12)             # the two dropped assignments
+    assert out[3] == pytest.approx(3 / (12 / 8))       # experts 1 and 2 carry 3 of a mean 1.5
+    assert mp[0] == pytest.approx(c) and mp[7] == pytest.approx(c)  # unused experts
+    assert mp[1] == pytest.approx((2 * a + b + 3 * c) / 6)
+
+
+def test_routing_stats_limits():
+    T, E, k = 64, 8, 1
+    # perfectly uniform routing: aux 1, entropy ln E, no imbalance
+    p = np.full((T, E), 1.0 / E, np.float32)
+    counts = np.full(E, T // E, np.int32)
+    out, mp = oracle.routing_stats(p, counts, counts, k)
+    assert out[0] == pytest.approx(1.0, rel=1e-6)
+    assert out[1] == pytest.approx(math.log(E), rel=1e-6)
+    assert out[2] == 0.0 and out[3] == pytest.approx(1.0)
+    assert np.allclose(mp, 1.0 / E)
+    # everything to expert 0 with certainty: aux E, entropy 0, imbalance E
+    p = np.zeros((T, E), np.float32)
+    p[:, 0] = 1.0
+    routed = np.zeros(E, np.int32)
+    routed[0] = T
+    kept = routed.copy()
+    kept[0] = T // 4
+    out, _ = oracle.routing_stats(p, routed, kept, k)
+    assert out[0] == pytest.approx(E) and out[1] == 0.0
+    assert out[2] == pytest.approx(0.75) and out[3] == pytest.approx(E)
+    # no tokens: all zero
+    out, _ = oracle.routing_stats(np.zeros((0, E), np.float32), np.zeros(E, np.int32),
+                                  np.zeros(E, np.int32), k)
+    assert (out == 0).all()
