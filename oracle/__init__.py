@@ -58,11 +58,11 @@ def _load():
         lib.oracle_capacity.argtypes = [i64, i32, i32, i32, dbl, P, P, P]
         lib.oracle_capacity.restype = i32
         lib.oracle_router_logits.argtypes = [i64, i32, i32, i32, P, P, P, P]
-        lib.oracle_softmax_topk.argtypes = [i64, i32, i32, P, P, P, P]
+        lib.oracle_softmax_topk.argtypes = [i64, i32, i32, i32, P, P, P, P]
         lib.oracle_assign.argtypes = [i64, i32, i32, i32, i64, i64] + [P] * 10
         lib.oracle_dispatch.argtypes = [i64, i32, i32, P, P, P]
         lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
-        lib.oracle_combine.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, P]
+        lib.oracle_combine.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, P, P]
         lib.oracle_token_outputs.argtypes = [i64, P, i32, i32, i32, i32, i32] + [P] * 9
         lib.oracle_routing_stats.argtypes = [i64, i32, i32, P, P, P, P, P]
         _lib = lib
@@ -79,6 +79,14 @@ def _host(t) -> Optional[np.ndarray]:
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
     return t.numpy()
+
+
+def _host_values(t) -> np.ndarray:
+    """Values of a fp32 or bf16 tensor as float64 on the host (exact)."""
+    a = _host(t)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
 
 
 def _ptr(a: Optional[np.ndarray]):
@@ -114,13 +122,13 @@ def router_logits(x, Wg, bias=None) -> np.ndarray:
     return g
 
 
-def softmax_topk(logits: np.ndarray, k: int, want_probs: bool = True):
+def softmax_topk(logits: np.ndarray, k: int, want_probs: bool = True, renorm: bool = False):
     g = np.ascontiguousarray(logits, dtype=np.float32)
     T, E = g.shape
     probs = np.empty((T, E), dtype=np.float32) if want_probs else None
     idx = np.empty((T, k), dtype=np.int32)
     gate = np.empty((T, k), dtype=np.float32)
-    _load().oracle_softmax_topk(T, E, k, _ptr(g), _ptr(probs), _ptr(idx), _ptr(gate))
+    _load().oracle_softmax_topk(T, E, k, int(renorm), _ptr(g), _ptr(probs), _ptr(idx), _ptr(gate))
     return probs, idx, gate
 
 
@@ -178,7 +186,7 @@ def expert_ffn(xd, expert_offsets: np.ndarray, W1, W3, W2, act: int) -> np.ndarr
 
 
 def combine(yd: np.ndarray, topk_idx, slot_pos, topk_gate, expert_offsets,
-            residual=None, dtype: int = F32) -> np.ndarray:
+            residual=None, dtype: int = F32, shared=None) -> np.ndarray:
     idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
     T, k = idx.shape
     d = yd.shape[1]
@@ -189,8 +197,9 @@ def combine(yd: np.ndarray, topk_idx, slot_pos, topk_gate, expert_offsets,
     gt = np.ascontiguousarray(topk_gate, np.float32)
     eo = np.ascontiguousarray(expert_offsets, np.int32)
     ydd = np.ascontiguousarray(yd, np.float64)
+    sh = None if shared is None else np.ascontiguousarray(shared, np.float64)
     _load().oracle_combine(T, d, k, dtype, _ptr(idx), _ptr(sp), _ptr(gt), _ptr(eo), _ptr(ydd),
-                           _ptr(ra), _ptr(y))
+                           _ptr(sh), _ptr(ra), _ptr(y))
     return y
 
 
@@ -207,10 +216,28 @@ def routing_stats(probs, counts_routed, counts_kept, k: int):
     return out, mp
 
 
+def shared_expert(x, Ws1, Ws3, Ws2, act: int) -> np.ndarray:
+    """A shared expert: the expert FFN applied to every token (one expert
+    whose rows are all T tokens in order)."""
+    xa = _host(x)
+    T = xa.shape[0]
+    w1, w3, w2 = _host(Ws1), _host(Ws3), _host(Ws2)
+    add = lambda a: None if a is None else a[None]  # one expert
+    return expert_ffn(xa, np.array([0, T], np.int32), add(w1), add(w3), add(w2), act)
+
+
 def token_outputs(tokens, x, topk_idx, slot_pos, topk_gate, W1, W3, W2, act: int,
-                  residual=None) -> np.ndarray:
-    """y[t] for the listed tokens, evaluated from the definition."""
+                  residual=None, shared=None) -> np.ndarray:
+    """y[t] for the listed tokens, evaluated from the definition; `shared`
+    = (Ws1, Ws3, Ws2) adds a shared expert after the routed sum, before the
+    residual."""
     toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.int64))
+    if shared is not None:
+        y = token_outputs(toks, x, topk_idx, slot_pos, topk_gate, W1, W3, W2, act)
+        y += shared_expert(_host(x)[toks], *shared, act)
+        if residual is not None:
+            y += _host_values(residual)[toks]
+        return y
     xa, w1, w3, w2, ra = _host(x), _host(W1), _host(W3), _host(W2), _host(residual)
     E, f, d = w1.shape
     k = topk_idx.shape[1]
@@ -236,9 +263,9 @@ class LayerResult:
     y: Optional[np.ndarray]
 
 
-def route(x, Wg, bias, k: int, want_probs: bool = True):
+def route(x, Wg, bias, k: int, want_probs: bool = True, renorm: bool = False):
     g = router_logits(x, Wg, bias)
-    probs, idx, gate = softmax_topk(g, k, want_probs)
+    probs, idx, gate = softmax_topk(g, k, want_probs, renorm)
     return g, probs, idx, gate
 
 

@@ -146,8 +146,13 @@ void oracle_router_logits(int64_t T, int d, int E, int dtype,
  * choice r is the softmax probability of that expert, not renormalised over
  * the k choices.  Softmax in double with the maximum subtracted, rounded to
  * fp32 once.
+ *
+ * With renorm set (the [NG] "Major Variants" top-2 combination read as a
+ * convex combination of the chosen experts): gate r is the softmax over the k
+ * chosen logits only, exp(g_r - m) / sum over chosen c of exp(g_c - m), so a
+ * token's k gates sum to one.
  * ------------------------------------------------------------------------ */
-void oracle_softmax_topk(int64_t T, int E, int k, const float* logits,
+void oracle_softmax_topk(int64_t T, int E, int k, int renorm, const float* logits,
                          float* probs /* [T, E] or NULL */,
                          int32_t* topk_idx /* [T, k] */,
                          float* topk_gate /* [T, k] */) {
@@ -162,6 +167,7 @@ void oracle_softmax_topk(int64_t T, int E, int k, const float* logits,
         /* chosen[] marks experts already taken by a higher rank */
         unsigned char chosen[1024];
         for (int e = 0; e < E; ++e) chosen[e] = 0;
+        double chosen_sum = 0.0;
         for (int r = 0; r < k; ++r) {
             int best = -1;
             for (int e = 0; e < E; ++e) {
@@ -170,7 +176,12 @@ void oracle_softmax_topk(int64_t T, int E, int k, const float* logits,
             }
             chosen[best] = 1;
             topk_idx[(size_t)t * k + r] = best;
-            topk_gate[(size_t)t * k + r] = (float)(exp((double)g[best] - m) / sum);
+            chosen_sum += exp((double)g[best] - m);
+        }
+        const double denom = renorm ? chosen_sum : sum;
+        for (int r = 0; r < k; ++r) {
+            const int e = topk_idx[(size_t)t * k + r];
+            topk_gate[(size_t)t * k + r] = (float)(exp((double)g[e] - m) / denom);
         }
         if (probs)
             for (int e = 0; e < E; ++e)
@@ -312,11 +323,16 @@ void oracle_expert_ffn(int E, int d, int f, int act, int dtype, const void* xd,
  * residual addition).  A dropped assignment adds nothing: the token passes
  * through the residual only ([NG] "Capacity Factor and Token Dropping").
  *     y[t] = residual[t] + sum over kept r of gate[t,r] * yd[row(t,r)]
- * residual NULL means no residual term.
+ * residual NULL means no residual term.  A shared expert ([NG] "Major
+ * Variants": a dense expert every token goes through, next to the routed
+ * ones) adds its output ys[t] after the routed sum and before the residual:
+ *     y[t] = residual[t] + (sum over kept r ... + ys[t])
+ * shared NULL means no shared expert.
  * ------------------------------------------------------------------------ */
 void oracle_combine(int64_t T, int d, int k, int dtype, const int32_t* topk_idx,
                     const int32_t* slot_pos, const float* topk_gate,
                     const int32_t* expert_offsets, const double* yd,
+                    const double* shared /* [T, d] or NULL */,
                     const void* residual, double* y /* [T, d] */) {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
@@ -328,6 +344,7 @@ void oracle_combine(int64_t T, int d, int k, int dtype, const int32_t* topk_idx,
                 int64_t row = (int64_t)expert_offsets[topk_idx[(size_t)t * k + r]] + pos;
                 s += (double)topk_gate[(size_t)t * k + r] * yd[(size_t)row * d + o];
             }
+            if (shared) s += shared[(size_t)t * d + o];
             if (residual) s += (double)elem(residual, dtype, (size_t)t * d + o);
             y[(size_t)t * d + o] = s;
         }

@@ -503,3 +503,58 @@ def test_routing_stats_limits():
     out, _ = oracle.routing_stats(np.zeros((0, E), np.float32), np.zeros(E, np.int32),
                                   np.zeros(E, np.int32), k)
     assert (out == 0).all()
+
+
+# --------------------------------------------------------------------------
+# renormalised top-k gates and the shared expert
+# --------------------------------------------------------------------------
+def test_renormalised_gates_closed_forms():
+    # worked example logits (3 at rank 0, 2 at rank 1, 0 elsewhere): the two
+    # renormalised gates are e^3/(e^3+e^2) = 1/(1+e^-1) and 1/(1+e)
+    g = np.zeros((6, 8), np.float32)
+    for t, (a, b) in enumerate([(1, 2), (2, 1), (1, 3), (2, 4), (3, 5), (4, 6)]):
+        g[t, a], g[t, b] = 3.0, 2.0
+    _, idx, gate = oracle.softmax_topk(g, 2, renorm=True)
+    _, idx0, _ = oracle.softmax_topk(g, 2)
+    assert np.array_equal(idx, idx0)  # renormalising changes no choice
+    assert np.allclose(gate[:, 0], 1 / (1 + math.exp(-1)), rtol=1e-7)
+    assert np.allclose(gate[:, 1], 1 / (1 + math.exp(1)), rtol=1e-7)
+    rng = np.random.default_rng(31)
+    g = (2 * rng.standard_normal((100, 16))).astype(np.float32)
+    # top-1: every gate is exactly one
+    _, _, gate1 = oracle.softmax_topk(g, 1, renorm=True)
+    assert (gate1 == 1.0).all()
+    # k = E: renormalising over every expert changes nothing
+    p_all, _, gate_all = oracle.softmax_topk(g, 16, renorm=True)
+    _, _, gate_plain = oracle.softmax_topk(g, 16)
+    np.testing.assert_allclose(gate_all, gate_plain, rtol=2e-7)
+    # a token's k gates sum to one
+    _, _, gate4 = oracle.softmax_topk(g, 4, renorm=True)
+    np.testing.assert_allclose(gate4.astype(np.float64).sum(axis=1), 1.0, rtol=1e-6)
+
+
+def test_shared_expert_against_dense_torch():
+    torch.manual_seed(41)
+    T, d, f = 37, 24, 40
+    x = torch.randn(T, d)
+    Ws1, Ws3 = torch.randn(f, d) / d**0.5, torch.randn(f, d) / d**0.5
+    Ws2 = torch.randn(d, f) / f**0.5
+    for act, w3 in ((oracle.SWIGLU, Ws3), (oracle.GELU, None)):
+        got = oracle.shared_expert(x, Ws1, w3, Ws2, act)
+        xd, a = x.double(), x.double() @ Ws1.double().T
+        hh = torch.nn.functional.silu(a) * (xd @ Ws3.double().T) if w3 is not None else \
+            torch.nn.functional.gelu(a)
+        np.testing.assert_allclose(got, (hh @ Ws2.double().T).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_combine_adds_shared_after_routed_before_residual():
+    # one token, one kept assignment with gate 1/2, values chosen so that the
+    # three terms are exact: y = (0.5 * 6) + 1.25 + 0.5 = 4.75
+    yd = np.array([[6.0]])
+    y = oracle.combine(yd, np.array([[0]]), np.array([[0]]), np.array([[0.5]], np.float32),
+                       np.array([0, 1]), residual=torch.tensor([[0.5]]), shared=np.array([[1.25]]))
+    assert y[0, 0] == 4.75
+    # a token whose only assignment was dropped gets shared + residual
+    y = oracle.combine(yd, np.array([[0]]), np.array([[-1]]), np.array([[0.5]], np.float32),
+                       np.array([0, 0]), residual=torch.tensor([[0.5]]), shared=np.array([[1.25]]))
+    assert y[0, 0] == 1.75
