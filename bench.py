@@ -251,6 +251,60 @@ def run_ours(args, rank, world, local_rank):
     kept = int(off[-1].item())
     n_dropped = int(dropped.item())
 
+    # ---- routing statistics (load-balancing term, entropy, drops, imbalance)
+    # from the router's probabilities: one captured call, timed like the others
+    probs = torch.empty(wl.T, wl.E, dtype=f32, device=dev)
+    moe.moe_route(p, inp.x, inp.Wg, inp.bias, idx, gate, probs, ws, wsb, None)
+    stats = torch.empty(moe.MOE_NUM_STATS, dtype=f32, device=dev)
+    mean_prob = torch.empty(wl.E, dtype=f32, device=dev)
+    stats_fn = lambda: moe.moe_routing_stats(p, probs, cr, ck, stats, mean_prob, ws, wsb, None)
+    stats_fn()
+    torch.cuda.synchronize(dev)
+    g_stats = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_stats):
+        stats_fn()
+    st_ev = []
+    for _ in range(args.steps):
+        flush()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        g_stats.replay()
+        b_ev.record(stream)
+        st_ev.append((a_ev, b_ev))
+    torch.cuda.synchronize(dev)
+    stats_ms = statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in st_ev)
+    stats_vals = stats.cpu().tolist()
+
+    # ---- a shared expert as wide as a routed one over every token (the
+    # layer option of moe_layer_forward_shared), timed alone like the calls
+    shared_ms = None
+    if wl.dtype == "bf16" and wl.act == "swiglu":
+        swl = wl.with_(ffn_shared=wl.ffn)
+        sp = moe.problem_of(swl)
+        sws = moe.alloc_workspace(sp, dev)
+        sin = moe_inputs.make_inputs(replica_workload(swl, rank), device=dev)
+        ys = torch.empty(wl.T, wl.d, dtype=inp.x.dtype, device=dev)
+        sh_fn = lambda: moe.moe_shared_expert_ffn(sp, sin.x, sin.Ws1, sin.Ws3, sin.Ws2, ys, sws, sws.numel(),
+                                                  None)
+        sh_fn()
+        torch.cuda.synchronize(dev)
+        g_sh = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_sh):
+            sh_fn()
+        sh_ev = []
+        for _ in range(args.steps):
+            flush()
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            g_sh.replay()
+            b_ev.record(stream)
+            sh_ev.append((a_ev, b_ev))
+        torch.cuda.synchronize(dev)
+        shared_ms = statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in sh_ev)
+        if moe.moe_device_status(sws, stream) != moe.MOE_OK:
+            raise RuntimeError("device status after the shared-expert loop")
+        del sin, sws, ys
+
     # ---- end to end through moe_layer_forward with host buffers
     x_host = inp.x.cpu().pin_memory()
     y_host = torch.empty(wl.T, wl.d, dtype=inp.x.dtype).pin_memory()
@@ -302,6 +356,13 @@ def run_ours(args, rank, world, local_rank):
                            "weight_GB_s": gb(weight_bytes, per_call["expert_ffn"])},
             "combine": {"ms": per_call["combine"], "GB_s": gb(combine_bytes, per_call["combine"]),
                         "frac_hbm": gb(combine_bytes, per_call["combine"]) / hbm_gbs},
+            "shared_expert_ffn": None if shared_ms is None else {
+                "ms": shared_ms, "ffn_shared": wl.ffn,
+                "TFLOP_s": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / 1e12,
+                "frac_bf16": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / (bf16_tf * 1e12)},
+            "routing_stats": {"ms": stats_ms, "GB_s": gb(wl.T * wl.E * 4 + 8 * wl.E, stats_ms),
+                              "aux": stats_vals[0], "entropy": stats_vals[1], "drop": stats_vals[2],
+                              "imbalance": stats_vals[3]},
         }
         value = job_tokens_per_s(wl.T, world, args.steps, total_ms_max)
         clocks = clk.summary()

@@ -22,6 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
+MOE_FLAG_RENORM = 1
 MOE_ACT_SWIGLU, MOE_ACT_GELU = 0, 1
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
@@ -29,19 +30,21 @@ MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe_route",
            "moe_assign_slots", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_device_status", "moe_status_string",
-           "moe_assign_slots_static")
+           "moe_assign_slots_static", "moe_routing_stats", "moe_shared_expert_ffn",
+           "moe_combine_shared", "moe_layer_forward_shared")
 
 
 class moe_problem(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("D", ctypes.c_int32), ("k", ctypes.c_int32), ("ffn", ctypes.c_int32),
                 ("capacity_factor", ctypes.c_double), ("dtype", ctypes.c_int32),
-                ("act", ctypes.c_int32)]
+                ("act", ctypes.c_int32), ("flags", ctypes.c_int32), ("ffn_shared", ctypes.c_int32)]
 
 
 _LAYOUT_FIELDS = ("status", "topk_idx", "topk_gate", "slot_pos", "counts_routed", "counts_kept",
                   "expert_offsets", "shard_offsets", "shard_routed", "shard_overflow", "dropped",
-                  "hist", "row_token", "xd", "h", "yd", "ffn_sync", "total")
+                  "hist", "row_token", "xd", "h", "yd", "ffn_sync", "stats", "hs", "ys", "shared_sync",
+                  "total")
 
 
 class moe_workspace_layout(ctypes.Structure):
@@ -80,6 +83,10 @@ def load() -> ctypes.CDLL:
     lib.moe_layer_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
     lib.moe_assign_slots_static.argtypes = [PP] + [P] * 11
     lib.moe_device_status.argtypes = [P, P]
+    lib.moe_routing_stats.argtypes = [PP, P, P, P, P, P, P, sz, P]
+    lib.moe_shared_expert_ffn.argtypes = [PP, P, P, P, P, P, P, sz, P]
+    lib.moe_combine_shared.argtypes = [PP, P, P, P, P, P, P, P, P, P]
+    lib.moe_layer_forward_shared.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for n in EXPORTS:
@@ -112,17 +119,20 @@ def _check(rc: int, where: str):
         raise MoeError(rc, where)
 
 
-def make_problem(T, d, E, D, k, ffn, capacity_factor, dtype="bf16", act="swiglu") -> moe_problem:
+def make_problem(T, d, E, D, k, ffn, capacity_factor, dtype="bf16", act="swiglu", renorm=False,
+                 ffn_shared=0) -> moe_problem:
     """moe_problem from plain values; dtype 'bf16'|'f32' (or code), act 'swiglu'|'gelu'."""
     dt = {"bf16": MOE_BF16, "f32": MOE_F32}.get(dtype, dtype)
     ac = {"swiglu": MOE_ACT_SWIGLU, "gelu": MOE_ACT_GELU}.get(act, act)
     return moe_problem(int(T), int(d), int(E), int(D), int(k), int(ffn), float(capacity_factor),
-                       int(dt), int(ac))
+                       int(dt), int(ac), MOE_FLAG_RENORM if renorm else 0, int(ffn_shared))
 
 
 def problem_of(wl) -> moe_problem:
-    """moe_problem from any object with T, d, E, D, k, ffn, capacity_factor, dtype, act."""
-    return make_problem(wl.T, wl.d, wl.E, wl.D, wl.k, wl.ffn, wl.capacity_factor, wl.dtype, wl.act)
+    """moe_problem from any object with T, d, E, D, k, ffn, capacity_factor, dtype, act
+    (and optionally renorm, ffn_shared)."""
+    return make_problem(wl.T, wl.d, wl.E, wl.D, wl.k, wl.ffn, wl.capacity_factor, wl.dtype, wl.act,
+                        getattr(wl, "renorm", False), getattr(wl, "ffn_shared", 0))
 
 
 # -------------------------------------------------------------- entries --
@@ -201,6 +211,35 @@ def moe_layer_forward(problem, x, Wg, bias, W1, W3, W2, residual, y, ws, ws_byte
     _check(load().moe_layer_forward(ctypes.byref(problem), _p(x), _p(Wg), _p(bias), _p(W1),
                                     _p(W3), _p(W2), _p(residual), _p(y), _p(ws), int(ws_bytes),
                                     _stream(stream)), "moe_layer_forward")
+
+
+MOE_STAT_AUX, MOE_STAT_ENTROPY, MOE_STAT_DROP, MOE_STAT_IMBALANCE, MOE_NUM_STATS = 0, 1, 2, 3, 4
+
+
+def moe_shared_expert_ffn(problem, x, Ws1, Ws3, Ws2, ys, ws, ws_bytes, stream=None):
+    _check(load().moe_shared_expert_ffn(ctypes.byref(problem), _p(x), _p(Ws1), _p(Ws3), _p(Ws2), _p(ys),
+                                        _p(ws), int(ws_bytes), _stream(stream)), "moe_shared_expert_ffn")
+
+
+def moe_combine_shared(problem, yd, topk_idx, slot_pos, expert_offsets, topk_gate, shared, residual, y,
+                       stream=None):
+    _check(load().moe_combine_shared(ctypes.byref(problem), _p(yd), _p(topk_idx), _p(slot_pos),
+                                     _p(expert_offsets), _p(topk_gate), _p(shared), _p(residual), _p(y),
+                                     _stream(stream)), "moe_combine_shared")
+
+
+def moe_layer_forward_shared(problem, x, Wg, bias, W1, W3, W2, Ws1, Ws3, Ws2, residual, y, ws, ws_bytes,
+                             stream=None):
+    _check(load().moe_layer_forward_shared(ctypes.byref(problem), _p(x), _p(Wg), _p(bias), _p(W1), _p(W3),
+                                           _p(W2), _p(Ws1), _p(Ws3), _p(Ws2), _p(residual), _p(y), _p(ws),
+                                           int(ws_bytes), _stream(stream)), "moe_layer_forward_shared")
+
+
+def moe_routing_stats(problem, probs, counts_routed, counts_kept, stats, mean_prob, ws, ws_bytes,
+                      stream=None):
+    _check(load().moe_routing_stats(ctypes.byref(problem), _p(probs), _p(counts_routed),
+                                    _p(counts_kept), _p(stats), _p(mean_prob), _p(ws), int(ws_bytes),
+                                    _stream(stream)), "moe_routing_stats")
 
 
 def moe_device_status(ws, stream=None) -> int:

@@ -40,9 +40,12 @@ int validate(const moe_problem* p) {
     if (!(p->capacity_factor > 0.0)) return MOE_ERR_INVALID_ARG;  // also rejects NaN
     if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (p->act != MOE_ACT_SWIGLU && p->act != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
+    if (p->flags & ~MOE_FLAG_RENORM) return MOE_ERR_INVALID_ARG;
+    if (p->ffn_shared < 0 || p->ffn_shared % 8) return MOE_ERR_INVALID_ARG;
     if (p->E > 256 || p->k > 8) return MOE_ERR_UNSUPPORTED;
     if (p->T * (int64_t)p->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)p->d * p->ffn >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)p->d * p->ffn_shared >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -57,9 +60,25 @@ int to_problem(const moe_problem* mp, Problem* p) {
     p->ffn = mp->ffn;
     p->dtype = mp->dtype;
     p->act = mp->act;
+    p->flags = mp->flags;
+    p->ffn_shared = mp->ffn_shared;
     capacity(mp, &p->C, &p->C_shard, &p->rows_max);
     p->nblk = ceil_div(p->T, kAssignBlock);
     return MOE_OK;
+}
+
+// The shared expert as a problem of its own: one expert whose rows are all T
+// tokens in order, width ffn_shared.
+Problem shared_problem(const Problem& p) {
+    Problem s = p;
+    s.E = 1;
+    s.D = 1;
+    s.k = 1;
+    s.ffn = p.ffn_shared;
+    s.C = p.T;
+    s.C_shard = p.T;
+    s.rows_max = p.T;
+    return s;
 }
 
 void layout(const Problem& p, moe_workspace_layout* L) {
@@ -87,6 +106,11 @@ void layout(const Problem& p, moe_workspace_layout* L) {
     L->h = take(rm * p.ffn * eb);
     L->yd = take(rm * p.d * eb);
     L->ffn_sync = take(ffn_sync_ints(p) * sizeof(int32_t));
+    L->stats = take((size_t)stats_blocks(p.T) * (size_t)(p.E + 1) * sizeof(double));
+    const size_t Ts = p.ffn_shared > 0 ? (size_t)p.T : 0;
+    L->hs = take(Ts * p.ffn_shared * eb);
+    L->ys = take(Ts * p.d * eb);
+    L->shared_sync = take(p.ffn_shared > 0 ? ffn_sync_ints(shared_problem(p)) * sizeof(int32_t) : 0);
     L->total = o;
 }
 
@@ -97,6 +121,76 @@ int check_ws(const Problem& p, void* ws, size_t ws_bytes, moe_workspace_layout* 
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// The shared expert's FFN over all T tokens (rows of x in order) into ys.
+int run_shared_expert(const Problem& p, const moe_workspace_layout& L, char* w, const void* x, const void* Ws1,
+                      const void* Ws3, const void* Ws2, void* ys, cudaStream_t s) {
+    const Problem sp = shared_problem(p);
+    void* hs = w + L.hs;
+    int* status = (int*)(w + L.status);
+    cudaError_t e;
+    if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
+        e = launch_ffn_tc(sp, x, nullptr, Ws1, Ws3, Ws2, hs, ys, status, (int*)(w + L.shared_sync), s);
+        if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+    } else {
+        e = launch_ffn_simt(sp, x, nullptr, Ws1, Ws3, Ws2, hs, ys, s);
+    }
+    return cuda_rc(e);
+}
+
+int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const float* bias, const void* W1,
+                  const void* W3, const void* W2, const void* Ws1, const void* Ws3, const void* Ws2,
+                  const void* residual, void* y, void* ws, size_t ws_bytes, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!x || !Wg || !W1 || !W2 || !y || (p.act == MOE_ACT_SWIGLU && !W3)) return MOE_ERR_INVALID_ARG;
+    const bool has_shared = p.ffn_shared > 0;
+    if (has_shared && (!Ws1 || !Ws2 || (p.act == MOE_ACT_SWIGLU && !Ws3))) return MOE_ERR_INVALID_ARG;
+    if (has_shared && (!aligned16(Ws1) || !aligned16(Ws2) || (Ws3 && !aligned16(Ws3))))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W2) || (W3 && !aligned16(W3)) ||
+        !aligned16(y) || (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) return MOE_OK;
+    char* w = (char*)ws;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t* idx = (int32_t*)(w + L.topk_idx);
+    float* gate = (float*)(w + L.topk_gate);
+    int32_t* slot = (int32_t*)(w + L.slot_pos);
+    int32_t* off = (int32_t*)(w + L.expert_offsets);
+    int32_t* row_token = (int32_t*)(w + L.row_token);
+    int* status = (int*)(w + L.status);
+    void *xd = w + L.xd, *h = w + L.h, *yd = w + L.yd;
+
+    int32_t* hist = (int32_t*)(w + L.hist);
+    // router + count pass (status[1] is the count pass's completion ticket), then the rank pass
+    const AssignScan scan{hist, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
+                          (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
+                          (int32_t*)(w + L.shard_overflow), (int32_t*)(w + L.dropped),
+                          (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C, p.C_shard};
+    cudaError_t e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
+    if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
+    if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
+    if (e == cudaSuccess) {
+        if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
+            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, (int*)(w + L.ffn_sync), s);
+            if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+        } else {
+            e = launch_ffn_simt(p, xd, off, W1, W3, W2, h, yd, s);
+        }
+    }
+    void* ys = has_shared ? (void*)(w + L.ys) : nullptr;
+    if (e == cudaSuccess && has_shared) {
+        const int rc2 = run_shared_expert(p, L, w, x, Ws1, Ws3, Ws2, ys, s);
+        if (rc2 != MOE_OK) return rc2;
+    }
+    if (e == cudaSuccess) e = launch_combine(p, yd, idx, slot, off, gate, residual, y, s, ys);
+    return cuda_rc(e);
+}
 
 }  // namespace
 }  // namespace moe
@@ -215,46 +309,63 @@ int moe_combine(const moe_problem* mp, const void* yd, const int32_t* topk_idx, 
 int moe_layer_forward(const moe_problem* mp, const void* x, const void* Wg, const float* bias, const void* W1,
                       const void* W3, const void* W2, const void* residual, void* y, void* ws, size_t ws_bytes,
                       void* stream) {
+    if (mp && mp->ffn_shared != 0) return MOE_ERR_INVALID_ARG;  // needs moe_layer_forward_shared
+    return layer_forward(mp, x, Wg, bias, W1, W3, W2, nullptr, nullptr, nullptr, residual, y, ws, ws_bytes,
+                         stream);
+}
+
+int moe_layer_forward_shared(const moe_problem* mp, const void* x, const void* Wg, const float* bias,
+                             const void* W1, const void* W3, const void* W2, const void* Ws1, const void* Ws3,
+                             const void* Ws2, const void* residual, void* y, void* ws, size_t ws_bytes,
+                             void* stream) {
+    return layer_forward(mp, x, Wg, bias, W1, W3, W2, Ws1, Ws3, Ws2, residual, y, ws, ws_bytes, stream);
+}
+
+int moe_shared_expert_ffn(const moe_problem* mp, const void* x, const void* Ws1, const void* Ws3,
+                          const void* Ws2, void* ys, void* ws, size_t ws_bytes, void* stream) {
     Problem p;
     int rc = to_problem(mp, &p);
     if (rc != MOE_OK) return rc;
-    if (!x || !Wg || !W1 || !W2 || !y || (p.act == MOE_ACT_SWIGLU && !W3)) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W2) || (W3 && !aligned16(W3)) ||
-        !aligned16(y) || (residual && !aligned16(residual)))
+    if (p.ffn_shared <= 0) return MOE_ERR_INVALID_ARG;
+    if (!x || !Ws1 || !Ws2 || !ys || (p.act == MOE_ACT_SWIGLU && !Ws3)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Ws1) || !aligned16(Ws2) || (Ws3 && !aligned16(Ws3)) || !aligned16(ys))
         return MOE_ERR_INVALID_ARG;
     moe_workspace_layout L;
     rc = check_ws(p, ws, ws_bytes, &L);
     if (rc != MOE_OK) return rc;
     if (p.T == 0) return MOE_OK;
-    char* w = (char*)ws;
-    cudaStream_t s = (cudaStream_t)stream;
-    int32_t* idx = (int32_t*)(w + L.topk_idx);
-    float* gate = (float*)(w + L.topk_gate);
-    int32_t* slot = (int32_t*)(w + L.slot_pos);
-    int32_t* off = (int32_t*)(w + L.expert_offsets);
-    int32_t* row_token = (int32_t*)(w + L.row_token);
-    int* status = (int*)(w + L.status);
-    void *xd = w + L.xd, *h = w + L.h, *yd = w + L.yd;
+    return run_shared_expert(p, L, (char*)ws, x, Ws1, Ws3, Ws2, ys, (cudaStream_t)stream);
+}
 
-    int32_t* hist = (int32_t*)(w + L.hist);
-    // router + count pass (status[1] is the count pass's completion ticket), then the rank pass
-    const AssignScan scan{hist, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
-                          (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
-                          (int32_t*)(w + L.shard_overflow), (int32_t*)(w + L.dropped),
-                          (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C, p.C_shard};
-    cudaError_t e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
-    if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
-    if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
-    if (e == cudaSuccess) {
-        if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
-            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, (int*)(w + L.ffn_sync), s);
-            if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
-        } else {
-            e = launch_ffn_simt(p, xd, off, W1, W3, W2, h, yd, s);
-        }
-    }
-    if (e == cudaSuccess) e = launch_combine(p, yd, idx, slot, off, gate, residual, y, s);
-    return cuda_rc(e);
+int moe_combine_shared(const moe_problem* mp, const void* yd, const int32_t* topk_idx, const int32_t* slot_pos,
+                       const int32_t* expert_offsets, const float* topk_gate, const void* shared,
+                       const void* residual, void* y, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) return MOE_OK;
+    if (!yd || !topk_idx || !slot_pos || !expert_offsets || !topk_gate || !y || !aligned16(yd) ||
+        !aligned16(y) || (residual && !aligned16(residual)) || (shared && !aligned16(shared)))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_combine(p, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y,
+                                  (cudaStream_t)stream, shared));
+}
+
+int moe_routing_stats(const moe_problem* mp, const float* probs, const int32_t* counts_routed,
+                      const int32_t* counts_kept, float* stats, float* mean_prob, void* ws, size_t ws_bytes,
+                      void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if ((p.T > 0 && !probs) || !counts_routed || !counts_kept || !stats) return MOE_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    char* w = (char*)ws;
+    // status[2] is the statistics kernel's completion ticket
+    return cuda_rc(launch_routing_stats(p, probs, counts_routed, counts_kept, stats, mean_prob,
+                                        (double*)(w + L.stats), (unsigned*)(w + L.status) + 2,
+                                        (cudaStream_t)stream));
 }
 
 int moe_device_status(void* ws, void* stream) {

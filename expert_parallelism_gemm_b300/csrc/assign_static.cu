@@ -75,6 +75,8 @@ extern "C" int moe_assign_slots_static(const moe_problem* mp, const int32_t* top
     p.ffn = mp->ffn;
     p.dtype = mp->dtype;
     p.act = mp->act;
+    p.flags = mp->flags;
+    p.ffn_shared = mp->ffn_shared;
     p.nblk = ceil_div(p.T, kAssignBlock);
     if ((p.T > 0 && (!topk_idx || !slot_pos || !row_token)) || !counts_routed || !counts_kept ||
         !expert_offsets || !shard_offsets || !shard_routed || !shard_overflow)

@@ -18,11 +18,13 @@ constexpr int kDevBadIndex = 2;  // an index read from memory was out of range
 
 constexpr int kThreads = 256;
 constexpr int kAssignBlock = 32;  // tokens per slot-assignment block (one warp)
+constexpr int kStatBlocks = 64;   // most CTAs (and partial sums) of the routing-statistics kernel
 
 struct Problem {
     int64_t T;
     int d, E, D, k, ffn;
     int dtype, act;
+    int flags, ffn_shared;
     int64_t C, C_shard, rows_max;
     int64_t nblk;  // ceil(T / kAssignBlock)
 };
@@ -153,9 +155,18 @@ cudaError_t launch_rank(const Problem& p, const int32_t* topk_idx, const int32_t
 cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_token,
                             const int32_t* expert_offsets, void* xd, cudaStream_t s);
 
+// shared: optional shared-expert output [T, d], added after the routed sum
 cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk_idx,
                            const int32_t* slot_pos, const int32_t* expert_offsets,
-                           const float* topk_gate, const void* residual, void* y, cudaStream_t s);
+                           const float* topk_gate, const void* residual, void* y, cudaStream_t s,
+                           const void* shared = nullptr);
+
+// routing statistics: `partials` holds stats_blocks(T) x (E+1) doubles,
+// `ticket` is zero before the launch and left zero
+int64_t stats_blocks(int64_t T);
+cudaError_t launch_routing_stats(const Problem& p, const float* probs, const int32_t* counts_routed,
+                                 const int32_t* counts_kept, float* stats, float* mean_prob,
+                                 double* partials, unsigned* ticket, cudaStream_t s);
 
 cudaError_t launch_ffn_simt(const Problem& p, const void* xd, const int32_t* expert_offsets,
                             const void* W1, const void* W3, const void* W2, void* h, void* yd,

@@ -26,9 +26,12 @@ ffn_simt_kernel(int N, int K, int64_t rows_max, const T* __restrict__ A,
     dep_wait();
     dep_release();
     const int e = blockIdx.z;
-    const int64_t r0 = (int64_t)expert_offsets[e] + (int64_t)blockIdx.x * BM;
+    // no offsets: one expert whose rows are 0..rows_max-1 (the shared expert)
+    const int64_t o0 = expert_offsets ? (int64_t)expert_offsets[e] : 0;
+    const int64_t o1 = expert_offsets ? (int64_t)expert_offsets[e + 1] : rows_max;
+    const int64_t r0 = o0 + (int64_t)blockIdx.x * BM;
     // rows never reach past rows_max, whatever the offsets say
-    const int64_t r1 = min((int64_t)expert_offsets[e + 1], rows_max);
+    const int64_t r1 = min(o1, rows_max);
     if (r0 < 0) return;
     if (r0 >= r1) return;
     const int n0 = blockIdx.y * BN;

@@ -98,7 +98,7 @@ struct FfnArgs {
     int n2, k2;    // down: n-tiles of 256 output columns per expert, k-blocks over ffn
     int mp_cap;    // bound on m-tile pairs per expert
     int lag;       // tiles placed between an expert's last gate/up tile and its down tiles
-    const int32_t* expert_offsets;
+    const int32_t* expert_offsets;  // null: one expert whose rows are 0..rows_max-1
     __nv_bfloat16* h;
     __nv_bfloat16* yd;
     int* status;
@@ -323,10 +323,12 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
         // expert offsets; they must be non-decreasing within [0, rows_max],
         // otherwise the kernel records kDevBadIndex and computes nothing
         bool bad = false;
+        // no offsets: one expert over all rows_max rows (the shared expert)
+        const int32_t* eo = args.expert_offsets;
         for (int e = lane; e <= E; e += 32) {
-            const int o = args.expert_offsets[e];
+            const int o = eo ? eo[e] : (e == 0 ? 0 : args.rows_max);
             S.offs[e] = o;
-            bad |= o < 0 || o > args.rows_max || (e > 0 && o < args.expert_offsets[e - 1]);
+            bad |= o < 0 || o > args.rows_max || (eo && e > 0 && o < eo[e - 1]);
         }
         bad = __any_sync(0xffffffffu, bad);
         __syncwarp();

@@ -9,7 +9,9 @@
 // Combine: same blog, phase 4 (results reassembled in token order); notes
 // page, expert combine (gate-weighted sum of a token's k outputs) and residual
 // addition.  One fixed order per token: fp32 fused multiply-adds over the
-// ranks in ascending order from +0, then the residual, then one rounding.
+// ranks in ascending order from +0, then the shared expert's output (notes
+// page, "Major Variants": a dense expert every token goes through), then the
+// residual, then one rounding.
 //
 // Both are HBM-bound copies: one warp per row or token, each lane moving 16
 // bytes per access, so a warp touches 512 contiguous bytes per instruction.
@@ -61,7 +63,7 @@ __global__ void __launch_bounds__(kThreads)
 combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __restrict__ yd,
                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_pos,
                const int32_t* __restrict__ expert_offsets, const float* __restrict__ topk_gate,
-               const T* __restrict__ residual, T* __restrict__ y) {
+               const T* __restrict__ shared, const T* __restrict__ residual, T* __restrict__ y) {
     dep_wait();
     dep_release();
     constexpr int VE = vec_elems<T>();
@@ -92,13 +94,14 @@ combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __res
         }
         for (int v0 = lane; v0 < nv; v0 += 32 * CB) {
             Vec16 q[CB][KM];
-            Vec16 rq[CB];
+            Vec16 rq[CB], sq[CB];
 #pragma unroll
             for (int c = 0; c < CB; ++c) {
                 const int v = v0 + 32 * c;
 #pragma unroll
                 for (int r = 0; r < KM; ++r)
                     if (rows[r] >= 0 && v < nv) q[c][r] = ld_nc_v16(yd + (size_t)rows[r] * d + v * VE);
+                if (shared && v < nv) sq[c] = ld_nc_v16(shared + (size_t)t * d + v * VE);
                 if (residual && v < nv) rq[c] = ld_nc_v16(residual + (size_t)t * d + v * VE);
             }
 #pragma unroll
@@ -115,6 +118,12 @@ combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __res
                     unpack(q[c][r], vals, (T*)nullptr);
 #pragma unroll
                     for (int j = 0; j < VE; ++j) acc[j] = fmaf(gates[r], vals[j], acc[j]);
+                }
+                if (shared) {
+                    float sv[8];
+                    unpack(sq[c], sv, (T*)nullptr);
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) acc[j] += sv[j];
                 }
                 if (residual) {
                     float rv[8];
@@ -149,24 +158,27 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_
 template <typename T>
 cudaError_t launch_combine_t(const Problem& p, unsigned g, const void* yd, const int32_t* topk_idx,
                              const int32_t* slot_pos, const int32_t* expert_offsets, const float* topk_gate,
-                             const void* residual, void* y, cudaStream_t s) {
+                             const void* shared, const void* residual, void* y, cudaStream_t s) {
     const T* ydt = (const T*)yd;
+    const T* st = (const T*)shared;
     const T* rt = (const T*)residual;
     T* yt = (T*)y;
     auto kern = p.k <= 2 ? combine_kernel<T, 4> : p.k <= 4 ? combine_kernel<T, 2> : combine_kernel<T, 1>;
     return launch_k(kern, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx,
-                    slot_pos, expert_offsets, topk_gate, rt, yt);
+                    slot_pos, expert_offsets, topk_gate, st, rt, yt);
 }
 
 cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk_idx,
                            const int32_t* slot_pos, const int32_t* expert_offsets,
-                           const float* topk_gate, const void* residual, void* y, cudaStream_t s) {
+                           const float* topk_gate, const void* residual, void* y, cudaStream_t s,
+                           const void* shared) {
     if (p.T == 0) return cudaSuccess;
     const unsigned g = grid_for(p.T);
     if (p.dtype == MOE_BF16)
         return launch_combine_t<__nv_bfloat16>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate,
-                                               residual, y, s);
-    return launch_combine_t<float>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y, s);
+                                               shared, residual, y, s);
+    return launch_combine_t<float>(p, g, yd, topk_idx, slot_pos, expert_offsets, topk_gate, shared, residual,
+                                   y, s);
 }
 
 }  // namespace moe

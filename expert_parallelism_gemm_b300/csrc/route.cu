@@ -30,7 +30,9 @@
 // experts, re-reading x from L2.
 //
 // Softmax and top-k run from a shared-memory logit table: one thread per token
-// for up to 32 experts, one warp per token above that.
+// for up to 32 experts, one warp per token above that.  The gate of choice r
+// is its softmax probability, or -- when renormalising -- exp(g_r - m) over
+// the sum of the k chosen exp(g - m), added in rank order.
 //
 // Inside the layer forward the router also starts the slot assignment: a CTA
 // holds exactly one assignment block of kAssignBlock tokens, so it counts its
@@ -86,6 +88,19 @@ __device__ __forceinline__ void rs_round(float (&a)[32], int lane) {
     }
 }
 
+// Gates of one token's k choices (chosen[r] = logit of choice r, m = the
+// token's largest logit, inv = 1 / sum over all experts of exp(g - m)).
+__device__ __forceinline__ void write_gates(float* gate, const float (&chosen)[8], int k, float m, float inv,
+                                            int renorm) {
+    if (!renorm) {
+        for (int r = 0; r < k; ++r) gate[r] = expf(chosen[r] - m) * inv;
+        return;
+    }
+    float den = 0.0f;
+    for (int r = 0; r < k; ++r) den += expf(chosen[r] - m);
+    for (int r = 0; r < k; ++r) gate[r] = expf(chosen[r] - m) / den;
+}
+
 template <typename T>
 __host__ __device__ constexpr int route_stages() {
     return sizeof(T) == 2 ? 4 : 3;
@@ -101,7 +116,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
              const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
-             float* __restrict__ topk_gate, float* __restrict__ probs, const AssignScan scan) {
+             float* __restrict__ topk_gate, float* __restrict__ probs, const int renorm,
+             const AssignScan scan) {
     constexpr int S = route_stages<T>();
     constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
     constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
@@ -206,6 +222,7 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
             if (probs)
                 for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = expf(gl[e] - m) * inv;
             uint32_t taken = 0;
+            float chosen[8];
             for (int r = 0; r < k; ++r) {
                 int be = -1;
                 float bv = -CUDART_INF_F;
@@ -217,10 +234,11 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                     }
                 }
                 taken |= 1u << be;
+                chosen[r] = bv;
                 topk_idx[(size_t)t * k + r] = be;
-                topk_gate[(size_t)t * k + r] = expf(bv - m) * inv;
                 if (count) atomicAdd(&cnt[r * E + be], 1);
             }
+            write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
         }
     } else {
         // softmax + top-k: one warp per token, lane holds experts lane + 32 q
@@ -253,6 +271,7 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                 }
             }
             uint32_t taken = 0;
+            float chosen[8];
             for (int r = 0; r < k; ++r) {
                 float bv = -CUDART_INF_F;
                 int be = 0x7fffffff;
@@ -275,12 +294,13 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                     }
                 }
                 if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                chosen[r] = bv;
                 if (lane == 0) {
                     topk_idx[(size_t)t * k + r] = be;
-                    topk_gate[(size_t)t * k + r] = expf(bv - m) * inv;
                     if (count) atomicAdd(&cnt[r * E + be], 1);
                 }
             }
+            if (lane == 0) write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
         }
     }
     if (count) {
@@ -304,7 +324,7 @@ cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, cons
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
     return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, p.T, p.d, p.E, p.k, (const T*)x,
-                    (const T*)Wg, bias, topk_idx, topk_gate, probs, scan);
+                    (const T*)Wg, bias, topk_idx, topk_gate, probs, (int)(p.flags & MOE_FLAG_RENORM), scan);
 }
 
 }  // namespace

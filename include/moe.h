@@ -68,7 +68,15 @@ typedef struct {
     double capacity_factor; /* c > 0, +INFINITY = never drop                  */
     int32_t dtype;          /* moe_dtype                                      */
     int32_t act;            /* moe_act                                        */
+    int32_t flags;          /* MOE_FLAG_* bits, 0 = none                      */
+    int32_t ffn_shared;     /* width of a shared expert (every token goes
+                               through it, next to the routed ones); 0 = none,
+                               else a multiple of 8                           */
 } moe_problem;
+
+/* flags: renormalise a token's k gates to sum to one (the softmax over the k
+ * chosen logits) instead of using the plain softmax probabilities. */
+#define MOE_FLAG_RENORM 1
 
 enum {
     MOE_OK = 0,
@@ -103,6 +111,10 @@ typedef struct {
     size_t ffn_sync;       /* int32 scratch of the expert FFN (gate/up ->
                               down release counters); every call leaves it
                               zero again                                    */
+    size_t stats;          /* double scratch of moe_routing_stats            */
+    size_t hs;             /* dtype[T * ffn_shared]: shared-expert hidden rows */
+    size_t ys;             /* dtype[T * d]: shared-expert outputs            */
+    size_t shared_sync;    /* int32 scratch of the shared-expert FFN         */
     size_t total;          /* = moe_workspace_size                           */
 } moe_workspace_layout;
 
@@ -132,7 +144,9 @@ int moe_workspace_layout_of(const moe_problem* p, moe_workspace_layout* out);
  *   probs[t] = softmax(g[t])            (temperature 1)
  *   topk_idx[t, r]  = the expert of rank r (largest logit first; equal logits
  *                     rank the lower expert first)
- *   topk_gate[t, r] = probs[t, topk_idx[t, r]]   (not renormalised)
+ *   topk_gate[t, r] = probs[t, topk_idx[t, r]]   (not renormalised), or with
+ *                     MOE_FLAG_RENORM the softmax over the k chosen logits
+ *                     (a token's k gates sum to one)
  * bias and probs may be NULL.  ws is unused (may be NULL). */
 int moe_route(const moe_problem* p, const void* x, const void* Wg, const float* bias,
               int32_t* topk_idx, float* topk_gate, float* probs,
@@ -198,6 +212,34 @@ int moe_layer_forward(const moe_problem* p, const void* x, const void* Wg, const
                       const void* W1, const void* W3, const void* W2, const void* residual,
                       void* y, void* ws, size_t ws_bytes, void* stream);
 
+/* Shared expert (notes page, "Major Variants": an expert every token goes
+ * through, next to the routed ones): ys[t] = FFN_shared(x[t]) for every
+ * token, the same FFN form as the routed experts (p->act) with width
+ * p->ffn_shared (> 0).  Ws1, Ws3: [ffn_shared, d] (Ws3 NULL for GELU);
+ * Ws2: [d, ffn_shared]; ys: [T, d] in the layer dtype.  bf16 SwiGLU runs on
+ * the same 2-SM tensor-core FFN kernel as the routed experts (one expert
+ * whose rows are x's rows).  Uses the workspace's hs and shared_sync regions. */
+int moe_shared_expert_ffn(const moe_problem* p, const void* x, const void* Ws1, const void* Ws3,
+                          const void* Ws2, void* ys, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_combine with the shared expert's output added after the routed sum
+ * and before the residual (both may be NULL):
+ *   y[t] = ((sum over kept r of gate * yd[row]) + shared[t]) + residual[t] */
+int moe_combine_shared(const moe_problem* p, const void* yd, const int32_t* topk_idx,
+                       const int32_t* slot_pos, const int32_t* expert_offsets,
+                       const float* topk_gate, const void* shared, const void* residual,
+                       void* y, void* stream);
+
+/* moe_layer_forward with a shared expert (p->ffn_shared > 0; its weights
+ * Ws1, Ws3, Ws2 as in moe_shared_expert_ffn): the routed layer, the shared
+ * expert over every token, and moe_combine_shared.  With p->ffn_shared == 0
+ * it is moe_layer_forward and the shared weights are ignored.
+ * moe_layer_forward itself rejects p->ffn_shared != 0. */
+int moe_layer_forward_shared(const moe_problem* p, const void* x, const void* Wg, const float* bias,
+                             const void* W1, const void* W3, const void* W2, const void* Ws1,
+                             const void* Ws3, const void* Ws2, const void* residual, void* y,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* Slot assignment without a workspace, for callers that cannot allocate
  * device memory (an operator inside a host framework that owns every device
  * allocation and passes only input and output buffers, or a latency-critical
@@ -220,6 +262,36 @@ int moe_assign_slots_static(const moe_problem* p, const int32_t* topk_idx, int32
                             int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
                             int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
                             int32_t* row_token, int32_t* dropped, void* stream);
+
+/* Indices of the moe_routing_stats outputs. */
+enum {
+    MOE_STAT_AUX = 0,       /* load-balancing term E * sum_e f_e * P_e       */
+    MOE_STAT_ENTROPY = 1,   /* mean routing entropy, nats                    */
+    MOE_STAT_DROP = 2,      /* dropped assignments / (T*k)                   */
+    MOE_STAT_IMBALANCE = 3, /* max_e routed_e / (T*k/E)                      */
+    MOE_NUM_STATS = 4
+};
+
+/* Routing statistics as device outputs (notes page, "Components and
+ * Architecture" and the formal algorithm's auxiliary load-balancing term:
+ * the share of tokens an expert receives times the share of router
+ * probability it receives, summed over experts; glossary page: the
+ * load-balancing loss; intro page, practitioner guidance: expert utilisation
+ * and routing entropy).  From the router probabilities of moe_route and the
+ * counts of moe_assign_slots:
+ *   f_e = counts_routed[e] / (T*k)   P_e = (1/T) sum_t probs[t,e]
+ *   stats[MOE_STAT_AUX]       = E * sum_e f_e * P_e   (1 = perfectly uniform)
+ *   stats[MOE_STAT_ENTROPY]   = (1/T) sum_t -sum_e p ln p  (0 ln 0 = 0)
+ *   stats[MOE_STAT_DROP]      = sum_e (counts_routed - counts_kept) / (T*k)
+ *   stats[MOE_STAT_IMBALANCE] = max_e counts_routed[e] / (T*k/E)
+ *   mean_prob[e]              = P_e                   (may be NULL)
+ * probs: [T, E] fp32, counts: [E] int32, stats: float[MOE_NUM_STATS], all
+ * device pointers.  Deterministic (fixed-order fp64 sums).  Uses the
+ * workspace's stats region and a ticket in its status region; T = 0 gives
+ * zeros. */
+int moe_routing_stats(const moe_problem* p, const float* probs, const int32_t* counts_routed,
+                      const int32_t* counts_kept, float* stats, float* mean_prob,
+                      void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, reads the workspace's device status word, clears it
  * and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if

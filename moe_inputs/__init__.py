@@ -56,6 +56,8 @@ class Workload:
     act: str = SWIGLU
     seed: int = 0
     zipf_s: Optional[float] = None  # skewed router bias; None = no bias
+    renorm: bool = False            # renormalise the k gates of a token to sum to one
+    ffn_shared: int = 0             # width of a shared expert every token goes through; 0 = none
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -95,11 +97,15 @@ class LayerInputs:
     W3: Optional[torch.Tensor]
     W2: torch.Tensor
     bias: Optional[torch.Tensor]
+    Ws1: Optional[torch.Tensor] = None  # shared expert [ffn_shared, d]
+    Ws3: Optional[torch.Tensor] = None  # [ffn_shared, d] (SwiGLU only)
+    Ws2: Optional[torch.Tensor] = None  # [d, ffn_shared]
 
     def to(self, device) -> "LayerInputs":
         mv = lambda t: None if t is None else t.to(device)
         return LayerInputs(self.wl, mv(self.x), mv(self.Wg), mv(self.W1),
-                           mv(self.W3), mv(self.W2), mv(self.bias))
+                           mv(self.W3), mv(self.W2), mv(self.bias), mv(self.Ws1), mv(self.Ws3),
+                           mv(self.Ws2))
 
 
 def torch_dtype(dtype: str) -> torch.dtype:
@@ -143,4 +149,11 @@ def make_inputs(wl: Workload, device="cpu") -> LayerInputs:
         rank = torch.empty(E, dtype=torch.float64, device=device)
         rank[perm] = torch.arange(1, E + 1, dtype=torch.float64, device=device)
         bias = (-wl.zipf_s * torch.log(rank)).to(torch.float32)
-    return LayerInputs(wl, x, Wg, W1, W3, W2, bias)
+    Ws1 = Ws3 = Ws2 = None
+    if wl.ffn_shared:
+        # drawn last, so the other tensors are the same with or without it
+        fs = wl.ffn_shared
+        Ws1 = _normal(gen, (fs, d), 1.0 / math.sqrt(d), wl.dtype, device)
+        Ws3 = _normal(gen, (fs, d), 1.0 / math.sqrt(d), wl.dtype, device) if wl.act == SWIGLU else None
+        Ws2 = _normal(gen, (d, fs), 1.0 / math.sqrt(fs), wl.dtype, device)
+    return LayerInputs(wl, x, Wg, W1, W3, W2, bias, Ws1, Ws3, Ws2)

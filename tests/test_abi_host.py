@@ -33,7 +33,7 @@ def _declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 16, names
     assert sorted(moe.EXPORTS) == names
     lib = moe.load()
     for n in names:
@@ -100,7 +100,8 @@ def test_workspace_layout_is_aligned_and_disjoint():
                      shard_offsets=4 * (wl.D + 1), shard_routed=4 * wl.D, shard_overflow=4 * wl.D,
                      dropped=4, hist=4 * wl.E * wl.k * nblk, row_token=4 * rows_max,
                      xd=eb * rows_max * wl.d, h=eb * rows_max * wl.ffn, yd=eb * rows_max * wl.d,
-                     ffn_sync=4 * (1 + wl.E * -(-(-(-C // 128)) // 2)))
+                     ffn_sync=4 * (1 + wl.E * -(-(-(-C // 128)) // 2)),
+                     stats=8 * min(64, max(1, -(-wl.T // 64))) * (wl.E + 1))
         spans = sorted((L[n], L[n] + s) for n, s in sizes.items())
         assert spans[0][0] == 0 == L["status"]
         for (a0, a1), (b0, b1) in zip(spans, spans[1:]):

@@ -243,6 +243,24 @@ def test_layer_equals_step_by_step(case):
                        y2.view(torch.int32 if y2.dtype == torch.float32 else torch.int16))
 
 
+def test_routing_stats(case):
+    """Load-balancing term, entropy, drop fraction, imbalance and mean
+    probabilities from the oracle's router probabilities and counts: within
+    1e-5 relative of the fp64 oracle."""
+    name, wl, dev, cpu, o = case
+    s = o["slots"]
+    stats = torch.full((moe.MOE_NUM_STATS,), -1.0, dtype=torch.float32, device="cuda")
+    mean_prob = torch.full((wl.E,), -1.0, dtype=torch.float32, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace ticket
+        moe.moe_routing_stats(dev.p, t_dev(o["probs"]), t_dev(s.counts_routed), t_dev(s.counts_kept),
+                              stats, mean_prob, dev.ws, dev.ws_bytes)
+        want, want_mp = oracle.routing_stats(o["probs"], s.counts_routed, s.counts_kept, wl.k)
+        np.testing.assert_allclose(stats.cpu().numpy().astype(np.float64), want, rtol=1e-5, atol=1e-7)
+        np.testing.assert_allclose(mean_prob.cpu().numpy().astype(np.float64), want_mp, rtol=1e-5,
+                                   atol=1e-9)
+    assert dev.status() == moe.MOE_OK
+
+
 def test_exact_ties_choose_the_lower_expert():
     # x = 0: every logit is exactly its bias, with ties
     wl = Workload("ties", T=96, d=64, E=16, D=4, k=3, ffn=64, capacity_factor=1.0, seed=30)
