@@ -65,6 +65,8 @@ def _load():
         lib.oracle_combine.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, P, P]
         lib.oracle_token_outputs.argtypes = [i64, P, i32, i32, i32, i32, i32] + [P] * 9
         lib.oracle_routing_stats.argtypes = [i64, i32, i32, P, P, P, P, P]
+        lib.oracle_expert_choice.argtypes = [i64, i32, i64, P, P, P]
+        lib.oracle_combine_expert_choice.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -224,6 +226,41 @@ def shared_expert(x, Ws1, Ws3, Ws2, act: int) -> np.ndarray:
     w1, w3, w2 = _host(Ws1), _host(Ws3), _host(Ws2)
     add = lambda a: None if a is None else a[None]  # one expert
     return expert_ffn(xa, np.array([0, T], np.int32), add(w1), add(w3), add(w2), act)
+
+
+@dataclass
+class ExpertChoice:
+    C: int                  # tokens per expert, min(C_expert, T)
+    row_token: np.ndarray   # [E * C]: expert e's tokens, ascending, at rows e*C ...
+    expert_offsets: np.ndarray  # [E + 1] = e * C
+    sel_row: np.ndarray     # [T, E]: row of (t, e), or -1
+
+
+def expert_choice(probs, capacity_factor: float, k: int, D: int = 1) -> ExpertChoice:
+    """Expert-choice routing: each expert takes its min(C, T) highest-probability
+    tokens (ties: lower token first), C from the capacity rule."""
+    pa = np.ascontiguousarray(probs, dtype=np.float32)
+    T, E = pa.shape
+    C, _, _ = capacity(T, k, E, D, capacity_factor)
+    Cc = min(C, T)
+    row_token = np.empty(E * Cc, dtype=np.int32)
+    sel_row = np.empty((T, E), dtype=np.int32)
+    _load().oracle_expert_choice(T, E, C, _ptr(pa), _ptr(row_token), _ptr(sel_row))
+    return ExpertChoice(Cc, row_token, np.arange(E + 1, dtype=np.int32) * Cc, sel_row)
+
+
+def combine_expert_choice(yd, probs, sel_row, residual=None, dtype: int = F32, shared=None) -> np.ndarray:
+    pa = np.ascontiguousarray(probs, dtype=np.float32)
+    T, E = pa.shape
+    sr = np.ascontiguousarray(sel_row, dtype=np.int32)
+    ydd = np.ascontiguousarray(yd, np.float64)
+    d = ydd.shape[1]
+    sh = None if shared is None else np.ascontiguousarray(shared, np.float64)
+    ra = _host(residual)
+    y = np.empty((T, d), dtype=np.float64)
+    _load().oracle_combine_expert_choice(T, d, E, dtype, _ptr(pa), _ptr(sr), _ptr(ydd), _ptr(sh), _ptr(ra),
+                                         _ptr(y))
+    return y
 
 
 def token_outputs(tokens, x, topk_idx, slot_pos, topk_gate, W1, W3, W2, act: int,

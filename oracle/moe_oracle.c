@@ -436,3 +436,84 @@ void oracle_routing_stats(int64_t T, int E, int k, const float* probs /* [T, E] 
     out[3] = Tk > 0.0 ? maxr / (Tk / (double)E) : 0.0;
     free(P);
 }
+
+/* ------------------------------------------------------------------------ *
+ * Expert-choice routing.  [NG] "Major Variants": instead of each token
+ * choosing its experts, each expert chooses its tokens, which balances the
+ * load by construction.
+ *
+ * Readings (the pages name the variant only): the router probabilities are
+ * the same per-token softmax; expert e takes the Cc = min(C, T) tokens with
+ * the largest probs[t, e], equal probabilities taken in ascending token order
+ * (C from the capacity rule, k read as the average number of experts per
+ * token); its rows are its tokens in ascending token order, at
+ * expert_offsets[e] = e * Cc; the weight of (t, e) is probs[t, e]; a token
+ * sums the outputs of the experts that took it in ascending expert order
+ * (none: 0, plus the residual).
+ * Outputs: row_token[e * Cc + j] = j-th token of expert e; sel_row[t*E + e]
+ * = its row, or -1 when e did not take t.
+ * ------------------------------------------------------------------------ */
+void oracle_expert_choice(int64_t T, int E, int64_t C, const float* probs,
+                          int32_t* row_token /* [E * min(C, T)] */,
+                          int32_t* sel_row /* [T, E] */) {
+    const int64_t Cc = C < T ? C : T;
+    for (int64_t i = 0; i < T * (int64_t)E; ++i) sel_row[i] = -1;
+#pragma omp parallel
+    {
+        int64_t* order = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T > 0 ? T : 1));
+        unsigned char* take = (unsigned char*)malloc((size_t)(T > 0 ? T : 1));
+#pragma omp for schedule(static)
+        for (int e = 0; e < E; ++e) {
+            /* selection sort by (probability descending, token ascending),
+               kept plain: the first Cc positions are the chosen tokens */
+            for (int64_t t = 0; t < T; ++t) {
+                order[t] = t;
+                take[t] = 0;
+            }
+            for (int64_t j = 0; j < Cc; ++j) {
+                int64_t best = j;
+                for (int64_t q = j + 1; q < T; ++q) {
+                    const float pb = probs[(size_t)order[best] * E + e];
+                    const float pq = probs[(size_t)order[q] * E + e];
+                    if (pq > pb || (pq == pb && order[q] < order[best])) best = q;
+                }
+                const int64_t tmp = order[j];
+                order[j] = order[best];
+                order[best] = tmp;
+                take[order[j]] = 1;
+            }
+            int64_t pos = 0;
+            for (int64_t t = 0; t < T; ++t) {
+                if (!take[t]) continue;
+                row_token[(size_t)e * Cc + pos] = (int32_t)t;
+                sel_row[(size_t)t * E + e] = (int32_t)(e * Cc + pos);
+                ++pos;
+            }
+        }
+        free(order);
+        free(take);
+    }
+}
+
+/* Combine for expert-choice routing: y[t] = sum over experts e that took t,
+ * in ascending e, of probs[t,e] * yd[sel_row[t,e]], plus the shared expert's
+ * output and the residual (each may be NULL), in double. */
+void oracle_combine_expert_choice(int64_t T, int d, int E, int dtype, const float* probs,
+                                  const int32_t* sel_row, const double* yd,
+                                  const double* shared, const void* residual,
+                                  double* y /* [T, d] */) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        for (int o = 0; o < d; ++o) {
+            double s = 0.0;
+            for (int e = 0; e < E; ++e) {
+                const int32_t row = sel_row[(size_t)t * E + e];
+                if (row < 0) continue;
+                s += (double)probs[(size_t)t * E + e] * yd[(size_t)row * d + o];
+            }
+            if (shared) s += shared[(size_t)t * d + o];
+            if (residual) s += (double)elem(residual, dtype, (size_t)t * d + o);
+            y[(size_t)t * d + o] = s;
+        }
+    }
+}

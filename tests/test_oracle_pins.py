@@ -558,3 +558,49 @@ def test_combine_adds_shared_after_routed_before_residual():
     y = oracle.combine(yd, np.array([[0]]), np.array([[-1]]), np.array([[0.5]], np.float32),
                        np.array([0, 0]), residual=torch.tensor([[0.5]]), shared=np.array([[1.25]]))
     assert y[0, 0] == 1.75
+
+
+# --------------------------------------------------------------------------
+# expert-choice routing
+# --------------------------------------------------------------------------
+def test_expert_choice_against_a_literal_sort():
+    rng = np.random.default_rng(61)
+    for T, E, k, c in ((40, 8, 2, 1.0), (33, 5, 1, 0.6), (17, 4, 3, 2.0), (9, 3, 1, 0.2)):
+        # probabilities on a coarse grid so that equal values (ties) occur
+        probs = (rng.integers(0, 6, size=(T, E)) / 8.0).astype(np.float32)
+        ec = oracle.expert_choice(probs, c, k)
+        C = oracle.capacity(T, k, E, 1, c)[0]
+        Cc = min(C, T)
+        assert ec.C == Cc and ec.row_token.shape == (E * Cc,)
+        for e in range(E):
+            want = sorted(range(T), key=lambda t: (-float(probs[t, e]), t))[:Cc]
+            assert ec.row_token[e * Cc:(e + 1) * Cc].tolist() == sorted(want)
+            for t in range(T):
+                row = ec.sel_row[t, e]
+                if t in want:
+                    assert ec.row_token[row] == t and e * Cc <= row < (e + 1) * Cc
+                else:
+                    assert row == -1
+
+
+def test_expert_choice_with_every_token_is_the_dense_soft_mixture():
+    # C >= T: every expert takes every token, so the layer is
+    # sum_e p_e FFN_e(x), evaluated here densely with torch
+    torch.manual_seed(62)
+    T, d, E, f = 21, 16, 4, 24
+    x = torch.randn(T, d)
+    W1, W3 = torch.randn(E, f, d) / d**0.5, torch.randn(E, f, d) / d**0.5
+    W2 = torch.randn(E, d, f) / f**0.5
+    g = (2 * torch.randn(T, E)).numpy().astype(np.float32)
+    probs, _, _ = oracle.softmax_topk(g, 1)
+    ec = oracle.expert_choice(probs, math.inf, 1)
+    assert ec.C == T and (ec.sel_row >= 0).all()
+    xd = oracle.dispatch(x, ec.row_token)
+    yd = oracle.expert_ffn(xd, ec.expert_offsets, W1, W3, W2, oracle.SWIGLU)
+    y = oracle.combine_expert_choice(yd, probs, ec.sel_row)
+    xx = x.double()
+    a = torch.einsum("td,efd->tef", xx, W1.double())
+    u = torch.einsum("td,efd->tef", xx, W3.double())
+    ye = torch.einsum("tef,edf->ted", torch.nn.functional.silu(a) * u, W2.double())
+    want = torch.einsum("te,ted->td", torch.from_numpy(probs).double(), ye)
+    np.testing.assert_allclose(y, want.numpy(), rtol=1e-9, atol=1e-12)
