@@ -236,10 +236,11 @@ class ExpertChoice:
     sel_row: np.ndarray     # [T, E]: row of (t, e), or -1
 
 
-def expert_choice(probs, capacity_factor: float, k: int, D: int = 1) -> ExpertChoice:
-    """Expert-choice routing: each expert takes its min(C, T) highest-probability
-    tokens (ties: lower token first), C from the capacity rule."""
-    pa = np.ascontiguousarray(probs, dtype=np.float32)
+def expert_choice(scores, capacity_factor: float, k: int, D: int = 1) -> ExpertChoice:
+    """Expert-choice routing: each expert takes its min(C, T) tokens of highest
+    score -- the fp32 router logit -- (ties: lower token first), C from the
+    capacity rule."""
+    pa = np.ascontiguousarray(scores, dtype=np.float32)
     T, E = pa.shape
     C, _, _ = capacity(T, k, E, D, capacity_factor)
     Cc = min(C, T)

@@ -442,18 +442,20 @@ void oracle_routing_stats(int64_t T, int E, int k, const float* probs /* [T, E] 
  * choosing its experts, each expert chooses its tokens, which balances the
  * load by construction.
  *
- * Readings (the pages name the variant only): the router probabilities are
- * the same per-token softmax; expert e takes the Cc = min(C, T) tokens with
- * the largest probs[t, e], equal probabilities taken in ascending token order
- * (C from the capacity rule, k read as the average number of experts per
- * token); its rows are its tokens in ascending token order, at
- * expert_offsets[e] = e * Cc; the weight of (t, e) is probs[t, e]; a token
- * sums the outputs of the experts that took it in ascending expert order
- * (none: 0, plus the residual).
+ * Readings (the pages name the variant only): expert e takes the
+ * Cc = min(C, T) tokens with the largest router score, the fp32 logit
+ * g[t, e] of the routing projection (the integer decision is taken on the
+ * same fp32 values the router computes, in its fixed order), equal scores
+ * taken in ascending token order (C from the capacity rule, k read as the
+ * average number of experts per token); its rows are its tokens in ascending
+ * token order, at expert_offsets[e] = e * Cc; the weight of (t, e) is the
+ * token's softmax probability probs[t, e]; a token sums the outputs of the
+ * experts that took it in ascending expert order (none: 0, plus the
+ * residual).
  * Outputs: row_token[e * Cc + j] = j-th token of expert e; sel_row[t*E + e]
  * = its row, or -1 when e did not take t.
  * ------------------------------------------------------------------------ */
-void oracle_expert_choice(int64_t T, int E, int64_t C, const float* probs,
+void oracle_expert_choice(int64_t T, int E, int64_t C, const float* score /* [T, E] */,
                           int32_t* row_token /* [E * min(C, T)] */,
                           int32_t* sel_row /* [T, E] */) {
     const int64_t Cc = C < T ? C : T;
@@ -464,8 +466,8 @@ void oracle_expert_choice(int64_t T, int E, int64_t C, const float* probs,
         unsigned char* take = (unsigned char*)malloc((size_t)(T > 0 ? T : 1));
 #pragma omp for schedule(static)
         for (int e = 0; e < E; ++e) {
-            /* selection sort by (probability descending, token ascending),
-               kept plain: the first Cc positions are the chosen tokens */
+            /* selection sort by (score descending, token ascending), kept
+               plain: the first Cc positions are the chosen tokens */
             for (int64_t t = 0; t < T; ++t) {
                 order[t] = t;
                 take[t] = 0;
@@ -473,8 +475,8 @@ void oracle_expert_choice(int64_t T, int E, int64_t C, const float* probs,
             for (int64_t j = 0; j < Cc; ++j) {
                 int64_t best = j;
                 for (int64_t q = j + 1; q < T; ++q) {
-                    const float pb = probs[(size_t)order[best] * E + e];
-                    const float pq = probs[(size_t)order[q] * E + e];
+                    const float pb = score[(size_t)order[best] * E + e];
+                    const float pq = score[(size_t)order[q] * E + e];
                     if (pq > pb || (pq == pb && order[q] < order[best])) best = q;
                 }
                 const int64_t tmp = order[j];

@@ -566,8 +566,9 @@ def test_combine_adds_shared_after_routed_before_residual():
 def test_expert_choice_against_a_literal_sort():
     rng = np.random.default_rng(61)
     for T, E, k, c in ((40, 8, 2, 1.0), (33, 5, 1, 0.6), (17, 4, 3, 2.0), (9, 3, 1, 0.2)):
-        # probabilities on a coarse grid so that equal values (ties) occur
-        probs = (rng.integers(0, 6, size=(T, E)) / 8.0).astype(np.float32)
+        # scores on a coarse grid (negative ones too, and -0) so ties occur
+        probs = (rng.integers(-3, 4, size=(T, E)) / 8.0).astype(np.float32)
+        probs[rng.random((T, E)) < 0.05] = -0.0
         ec = oracle.expert_choice(probs, c, k)
         C = oracle.capacity(T, k, E, 1, c)[0]
         Cc = min(C, T)
@@ -593,7 +594,7 @@ def test_expert_choice_with_every_token_is_the_dense_soft_mixture():
     W2 = torch.randn(E, d, f) / f**0.5
     g = (2 * torch.randn(T, E)).numpy().astype(np.float32)
     probs, _, _ = oracle.softmax_topk(g, 1)
-    ec = oracle.expert_choice(probs, math.inf, 1)
+    ec = oracle.expert_choice(g, math.inf, 1)
     assert ec.C == T and (ec.sel_row >= 0).all()
     xd = oracle.dispatch(x, ec.row_token)
     yd = oracle.expert_ffn(xd, ec.expert_offsets, W1, W3, W2, oracle.SWIGLU)
