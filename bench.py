@@ -305,6 +305,33 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError("device status after the shared-expert loop")
         del sin, sws, ys
 
+    # ---- the same layer with expert-choice routing (each expert takes its
+    # C highest-scoring tokens), one whole moe_layer_forward per replay
+    ewl = wl.with_(expert_choice=True)
+    ep = moe.problem_of(ewl)
+    ews = moe.alloc_workspace(ep, dev)
+    ec_fn = lambda: moe.moe_layer_forward(ep, inp.x, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y, ews,
+                                          ews.numel(), None)
+    ec_fn()
+    torch.cuda.synchronize(dev)
+    g_ec = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_ec):
+        ec_fn()
+    ec_ev = []
+    for _ in range(args.steps):
+        flush()
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_ev.record(stream)
+        g_ec.replay()
+        b_ev.record(stream)
+        ec_ev.append((a_ev, b_ev))
+    torch.cuda.synchronize(dev)
+    ec_ms = statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in ec_ev)
+    if moe.moe_device_status(ews, stream) != moe.MOE_OK:
+        raise RuntimeError("device status after the expert-choice loop")
+    ec_rows = ewl.E * moe.moe_capacity(ep)[0]
+    del ews
+
     # ---- end to end through moe_layer_forward with host buffers
     x_host = inp.x.cpu().pin_memory()
     y_host = torch.empty(wl.T, wl.d, dtype=inp.x.dtype).pin_memory()
@@ -360,6 +387,8 @@ def run_ours(args, rank, world, local_rank):
                 "ms": shared_ms, "ffn_shared": wl.ffn,
                 "TFLOP_s": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / 1e12,
                 "frac_bf16": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / (bf16_tf * 1e12)},
+            "expert_choice_layer": {"ms": ec_ms, "tokens_per_s": wl.T / (ec_ms * 1e-3), "rows": ec_rows,
+                                    "note": "whole moe_layer_forward with expert-choice routing, graph replay"},
             "routing_stats": {"ms": stats_ms, "GB_s": gb(wl.T * wl.E * 4 + 8 * wl.E, stats_ms),
                               "aux": stats_vals[0], "entropy": stats_vals[1], "drop": stats_vals[2],
                               "imbalance": stats_vals[3]},

@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
-MOE_FLAG_RENORM = 1
+MOE_FLAG_RENORM, MOE_FLAG_EXPERT_CHOICE = 1, 2
 MOE_ACT_SWIGLU, MOE_ACT_GELU = 0, 1
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
@@ -31,7 +31,8 @@ EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe
            "moe_assign_slots", "moe_dispatch", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_device_status", "moe_status_string",
            "moe_assign_slots_static", "moe_routing_stats", "moe_shared_expert_ffn",
-           "moe_combine_shared", "moe_layer_forward_shared")
+           "moe_combine_shared", "moe_layer_forward_shared", "moe_expert_choice_assign",
+           "moe_combine_expert_choice", "moe_router_logits")
 
 
 class moe_problem(ctypes.Structure):
@@ -44,7 +45,7 @@ class moe_problem(ctypes.Structure):
 _LAYOUT_FIELDS = ("status", "topk_idx", "topk_gate", "slot_pos", "counts_routed", "counts_kept",
                   "expert_offsets", "shard_offsets", "shard_routed", "shard_overflow", "dropped",
                   "hist", "row_token", "xd", "h", "yd", "ffn_sync", "stats", "hs", "ys", "shared_sync",
-                  "total")
+                  "probs", "logits", "sel_row", "total")
 
 
 class moe_workspace_layout(ctypes.Structure):
@@ -87,6 +88,9 @@ def load() -> ctypes.CDLL:
     lib.moe_shared_expert_ffn.argtypes = [PP, P, P, P, P, P, P, sz, P]
     lib.moe_combine_shared.argtypes = [PP, P, P, P, P, P, P, P, P, P]
     lib.moe_layer_forward_shared.argtypes = [PP, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.moe_expert_choice_assign.argtypes = [PP, P, P, P, P, P]
+    lib.moe_router_logits.argtypes = [PP, P, P, P, P, P, P]
+    lib.moe_combine_expert_choice.argtypes = [PP, P, P, P, P, P, P, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for n in EXPORTS:
@@ -120,19 +124,22 @@ def _check(rc: int, where: str):
 
 
 def make_problem(T, d, E, D, k, ffn, capacity_factor, dtype="bf16", act="swiglu", renorm=False,
-                 ffn_shared=0) -> moe_problem:
+                 ffn_shared=0, expert_choice=False) -> moe_problem:
     """moe_problem from plain values; dtype 'bf16'|'f32' (or code), act 'swiglu'|'gelu'."""
     dt = {"bf16": MOE_BF16, "f32": MOE_F32}.get(dtype, dtype)
     ac = {"swiglu": MOE_ACT_SWIGLU, "gelu": MOE_ACT_GELU}.get(act, act)
     return moe_problem(int(T), int(d), int(E), int(D), int(k), int(ffn), float(capacity_factor),
-                       int(dt), int(ac), MOE_FLAG_RENORM if renorm else 0, int(ffn_shared))
+                       int(dt), int(ac),
+                       (MOE_FLAG_RENORM if renorm else 0) | (MOE_FLAG_EXPERT_CHOICE if expert_choice else 0),
+                       int(ffn_shared))
 
 
 def problem_of(wl) -> moe_problem:
     """moe_problem from any object with T, d, E, D, k, ffn, capacity_factor, dtype, act
     (and optionally renorm, ffn_shared)."""
     return make_problem(wl.T, wl.d, wl.E, wl.D, wl.k, wl.ffn, wl.capacity_factor, wl.dtype, wl.act,
-                        getattr(wl, "renorm", False), getattr(wl, "ffn_shared", 0))
+                        getattr(wl, "renorm", False), getattr(wl, "ffn_shared", 0),
+                        getattr(wl, "expert_choice", False))
 
 
 # -------------------------------------------------------------- entries --
@@ -226,6 +233,21 @@ def moe_combine_shared(problem, yd, topk_idx, slot_pos, expert_offsets, topk_gat
     _check(load().moe_combine_shared(ctypes.byref(problem), _p(yd), _p(topk_idx), _p(slot_pos),
                                      _p(expert_offsets), _p(topk_gate), _p(shared), _p(residual), _p(y),
                                      _stream(stream)), "moe_combine_shared")
+
+
+def moe_router_logits(problem, x, Wg, bias, logits, probs, stream=None):
+    _check(load().moe_router_logits(ctypes.byref(problem), _p(x), _p(Wg), _p(bias), _p(logits), _p(probs),
+                                    _stream(stream)), "moe_router_logits")
+
+
+def moe_expert_choice_assign(problem, logits, row_token, expert_offsets, sel_row, stream=None):
+    _check(load().moe_expert_choice_assign(ctypes.byref(problem), _p(logits), _p(row_token), _p(expert_offsets),
+                                           _p(sel_row), _stream(stream)), "moe_expert_choice_assign")
+
+
+def moe_combine_expert_choice(problem, yd, probs, sel_row, shared, residual, y, stream=None):
+    _check(load().moe_combine_expert_choice(ctypes.byref(problem), _p(yd), _p(probs), _p(sel_row), _p(shared),
+                                            _p(residual), _p(y), _stream(stream)), "moe_combine_expert_choice")
 
 
 def moe_layer_forward_shared(problem, x, Wg, bias, W1, W3, W2, Ws1, Ws3, Ws2, residual, y, ws, ws_bytes,

@@ -28,7 +28,7 @@ int capacity(const moe_problem* p, int64_t* C, int64_t* Cs, int64_t* rows_max) {
         *C = ve >= (double)p->T ? p->T : (int64_t)ve;
         *Cs = vs >= (double)Tk ? Tk : (int64_t)vs;
     }
-    *rows_max = std::min<int64_t>((int64_t)p->E * *C, Tk);
+    *rows_max = (p->flags & MOE_FLAG_EXPERT_CHOICE) ? (int64_t)p->E * *C : std::min<int64_t>((int64_t)p->E * *C, Tk);
     return MOE_OK;
 }
 
@@ -40,12 +40,16 @@ int validate(const moe_problem* p) {
     if (!(p->capacity_factor > 0.0)) return MOE_ERR_INVALID_ARG;  // also rejects NaN
     if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (p->act != MOE_ACT_SWIGLU && p->act != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
-    if (p->flags & ~MOE_FLAG_RENORM) return MOE_ERR_INVALID_ARG;
+    if (p->flags & ~(MOE_FLAG_RENORM | MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
+    if ((p->flags & MOE_FLAG_RENORM) && (p->flags & MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
     if (p->ffn_shared < 0 || p->ffn_shared % 8) return MOE_ERR_INVALID_ARG;
     if (p->E > 256 || p->k > 8) return MOE_ERR_UNSUPPORTED;
     if (p->T * (int64_t)p->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)p->d * p->ffn >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)p->d * p->ffn_shared >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    // expert choice keeps an expert's probability column in shared memory
+    if ((p->flags & MOE_FLAG_EXPERT_CHOICE) && p->T > 49152) return MOE_ERR_UNSUPPORTED;
+    if ((p->flags & MOE_FLAG_EXPERT_CHOICE) && p->T * (int64_t)p->E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -111,6 +115,10 @@ void layout(const Problem& p, moe_workspace_layout* L) {
     L->hs = take(Ts * p.ffn_shared * eb);
     L->ys = take(Ts * p.d * eb);
     L->shared_sync = take(p.ffn_shared > 0 ? ffn_sync_ints(shared_problem(p)) * sizeof(int32_t) : 0);
+    const size_t TE = (p.flags & MOE_FLAG_EXPERT_CHOICE) ? (size_t)p.T * p.E : 0;
+    L->probs = take(TE * sizeof(float));
+    L->logits = take(TE * sizeof(float));
+    L->sel_row = take(TE * sizeof(int32_t));
     L->total = o;
 }
 
@@ -167,13 +175,25 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
     void *xd = w + L.xd, *h = w + L.h, *yd = w + L.yd;
 
     int32_t* hist = (int32_t*)(w + L.hist);
-    // router + count pass (status[1] is the count pass's completion ticket), then the rank pass
-    const AssignScan scan{hist, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
-                          (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
-                          (int32_t*)(w + L.shard_overflow), (int32_t*)(w + L.dropped),
-                          (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C, p.C_shard};
-    cudaError_t e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
-    if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
+    const bool ec = (p.flags & MOE_FLAG_EXPERT_CHOICE) != 0;
+    float* probs = (float*)(w + L.probs);
+    float* logits = (float*)(w + L.logits);
+    int32_t* sel_row = (int32_t*)(w + L.sel_row);
+    cudaError_t e;
+    if (ec) {
+        // expert choice: router logits and probabilities, then each expert
+        // takes its tokens by logit
+        e = launch_route(p, x, Wg, bias, nullptr, nullptr, probs, s, logits);
+        if (e == cudaSuccess) e = launch_ec_select(p, logits, row_token, off, sel_row, s);
+    } else {
+        // router + count pass (status[1] is the count pass's completion ticket), then the rank pass
+        const AssignScan scan{hist, (int32_t*)(w + L.counts_routed), (int32_t*)(w + L.counts_kept), off,
+                              (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
+                              (int32_t*)(w + L.shard_overflow), (int32_t*)(w + L.dropped),
+                              (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C, p.C_shard};
+        e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
+        if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
+    }
     if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
     if (e == cudaSuccess) {
         if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
@@ -188,7 +208,9 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
         const int rc2 = run_shared_expert(p, L, w, x, Ws1, Ws3, Ws2, ys, s);
         if (rc2 != MOE_OK) return rc2;
     }
-    if (e == cudaSuccess) e = launch_combine(p, yd, idx, slot, off, gate, residual, y, s, ys);
+    if (e == cudaSuccess)
+        e = ec ? launch_ec_combine(p, yd, probs, sel_row, ys, residual, y, s)
+               : launch_combine(p, yd, idx, slot, off, gate, residual, y, s, ys);
     return cuda_rc(e);
 }
 
@@ -349,6 +371,39 @@ int moe_combine_shared(const moe_problem* mp, const void* yd, const int32_t* top
         return MOE_ERR_INVALID_ARG;
     return cuda_rc(launch_combine(p, yd, topk_idx, slot_pos, expert_offsets, topk_gate, residual, y,
                                   (cudaStream_t)stream, shared));
+}
+
+int moe_router_logits(const moe_problem* mp, const void* x, const void* Wg, const float* bias, float* logits,
+                      float* probs, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) return MOE_OK;
+    if (!x || !Wg || !logits || !aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_route(p, x, Wg, bias, nullptr, nullptr, probs, (cudaStream_t)stream, logits));
+}
+
+int moe_expert_choice_assign(const moe_problem* mp, const float* logits, int32_t* row_token,
+                             int32_t* expert_offsets, int32_t* sel_row, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!(p.flags & MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
+    if (!expert_offsets || (p.T > 0 && (!logits || !row_token || !sel_row))) return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_ec_select(p, logits, row_token, expert_offsets, sel_row, (cudaStream_t)stream));
+}
+
+int moe_combine_expert_choice(const moe_problem* mp, const void* yd, const float* probs, const int32_t* sel_row,
+                              const void* shared, const void* residual, void* y, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!(p.flags & MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
+    if (p.T == 0) return MOE_OK;
+    if (!yd || !probs || !sel_row || !y || !aligned16(yd) || !aligned16(y) || (shared && !aligned16(shared)) ||
+        (residual && !aligned16(residual)))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_ec_combine(p, yd, probs, sel_row, shared, residual, y, (cudaStream_t)stream));
 }
 
 int moe_routing_stats(const moe_problem* mp, const float* probs, const int32_t* counts_routed,

@@ -131,8 +131,10 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 }
 
 // ---- launchers (each returns cudaGetLastError() of its launches) ----------
+// logits (optional): the fp32 router logits [T, E], bias included
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
-                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s);
+                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s,
+                         float* logits = nullptr);
 
 // router plus the count pass of the slot assignment (hist and scan outputs in
 // `scan`, defined in assign_scan.cuh); T must be > 0
@@ -167,6 +169,12 @@ int64_t stats_blocks(int64_t T);
 cudaError_t launch_routing_stats(const Problem& p, const float* probs, const int32_t* counts_routed,
                                  const int32_t* counts_kept, float* stats, float* mean_prob,
                                  double* partials, unsigned* ticket, cudaStream_t s);
+
+// expert-choice routing (ec.cu)
+cudaError_t launch_ec_select(const Problem& p, const float* logits, int32_t* row_token, int32_t* expert_offsets,
+                             int32_t* sel_row, cudaStream_t s);
+cudaError_t launch_ec_combine(const Problem& p, const void* yd, const float* probs, const int32_t* sel_row,
+                              const void* shared, const void* residual, void* y, cudaStream_t s);
 
 cudaError_t launch_ffn_simt(const Problem& p, const void* xd, const int32_t* expert_offsets,
                             const void* W1, const void* W3, const void* W2, void* h, void* yd,

@@ -116,8 +116,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
              const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
-             float* __restrict__ topk_gate, float* __restrict__ probs, const int renorm,
-             const AssignScan scan) {
+             float* __restrict__ topk_gate, float* __restrict__ probs, float* __restrict__ logits,
+             const int renorm, const AssignScan scan) {
     constexpr int S = route_stages<T>();
     constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
     constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
@@ -198,7 +198,11 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
             rs_round<1, 2>(acc, lane);
             const int tl = kRT * warp + (lane >> 3);
             const int e = pass * kRE + (lane & 7);
-            if (e < E) lg[tl * LGP + e] = bias ? acc[0] + bias[e] : acc[0];
+            if (e < E) {
+                const float g = bias ? acc[0] + bias[e] : acc[0];
+                lg[tl * LGP + e] = g;
+                if (logits && t0 + tl < T_) logits[(size_t)(t0 + tl) * E + e] = g;
+            }
 #pragma unroll
             for (int p = 0; p < 32; ++p) acc[p] = 0.0f;
         }
@@ -235,10 +239,10 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                 }
                 taken |= 1u << be;
                 chosen[r] = bv;
-                topk_idx[(size_t)t * k + r] = be;
+                if (topk_idx) topk_idx[(size_t)t * k + r] = be;
                 if (count) atomicAdd(&cnt[r * E + be], 1);
             }
-            write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
+            if (topk_gate) write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
         }
     } else {
         // softmax + top-k: one warp per token, lane holds experts lane + 32 q
@@ -296,11 +300,11 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                 if ((be & 31) == lane) taken |= 1u << (be >> 5);
                 chosen[r] = bv;
                 if (lane == 0) {
-                    topk_idx[(size_t)t * k + r] = be;
+                    if (topk_idx) topk_idx[(size_t)t * k + r] = be;
                     if (count) atomicAdd(&cnt[r * E + be], 1);
                 }
             }
-            if (lane == 0) write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
+            if (lane == 0 && topk_gate) write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
         }
     }
     if (count) {
@@ -316,26 +320,27 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
 
 template <typename T>
 cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
-                           int32_t* topk_idx, float* topk_gate, float* probs, const AssignScan& scan,
-                           cudaStream_t s) {
+                           int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
+                           const AssignScan& scan, cudaStream_t s) {
     const size_t smem = route_smem_bytes((int)sizeof(T), route_stages<T>(), p.E, p.k);
     auto kern = route_kernel<T>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
     return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, p.T, p.d, p.E, p.k, (const T*)x,
-                    (const T*)Wg, bias, topk_idx, topk_gate, probs, (int)(p.flags & MOE_FLAG_RENORM), scan);
+                    (const T*)Wg, bias, topk_idx, topk_gate, probs, logits, (int)(p.flags & MOE_FLAG_RENORM),
+                    scan);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
-                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s) {
+                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s, float* logits) {
     if (p.T == 0) return cudaSuccess;
     AssignScan none{};
     if (p.dtype == MOE_BF16)
-        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, none, s);
-    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, none, s);
+        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, none, s);
+    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, none, s);
 }
 
 cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
@@ -343,8 +348,8 @@ cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, 
                                cudaStream_t s) {
     if (p.T == 0) return cudaErrorInvalidValue;  // callers handle T = 0 without a launch
     if (p.dtype == MOE_BF16)
-        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, scan, s);
-    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, scan, s);
+        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, scan, s);
+    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, scan, s);
 }
 
 }  // namespace moe

@@ -77,6 +77,12 @@ typedef struct {
 /* flags: renormalise a token's k gates to sum to one (the softmax over the k
  * chosen logits) instead of using the plain softmax probabilities. */
 #define MOE_FLAG_RENORM 1
+/* flags: expert-choice routing -- each expert takes its min(C, T) tokens of
+ * highest router probability (ties: lower token first) instead of each token
+ * taking its top-k experts; k is read as the average number of experts per
+ * token in the capacity rule.  Not combinable with MOE_FLAG_RENORM; needs
+ * T <= 49152. */
+#define MOE_FLAG_EXPERT_CHOICE 2
 
 enum {
     MOE_OK = 0,
@@ -115,6 +121,11 @@ typedef struct {
     size_t hs;             /* dtype[T * ffn_shared]: shared-expert hidden rows */
     size_t ys;             /* dtype[T * d]: shared-expert outputs            */
     size_t shared_sync;    /* int32 scratch of the shared-expert FFN         */
+    size_t probs;          /* float[T * E]: router probabilities (expert-choice
+                              layer forward only)                           */
+    size_t logits;         /* float[T * E]: router logits (expert-choice
+                              layer forward only)                           */
+    size_t sel_row;        /* int32[T * E]: expert-choice row of (t, e) or -1 */
     size_t total;          /* = moe_workspace_size                           */
 } moe_workspace_layout;
 
@@ -125,7 +136,8 @@ typedef struct {
  *   *C_expert = min(T, ceil((T*k/E)*c))   (c = inf: T)
  *   *C_shard  = min(T*k, ceil((T*k/D)*c)) (c = inf: T*k), used for the
  *               per-shard overflow max(0, routed_s - C_shard)
- *   *rows_max = min(E*C_expert, T*k), the bound on kept assignments.
+ *   *rows_max = min(E*C_expert, T*k), the bound on kept assignments
+ *               (expert-choice routing: exactly E*C_expert rows).
  * Host-only; no CUDA call.  Returns MOE_ERR_INVALID_ARG on a bad problem. */
 int moe_capacity(const moe_problem* p, int64_t* C_expert, int64_t* C_shard,
                  int64_t* rows_max);
@@ -239,6 +251,34 @@ int moe_layer_forward_shared(const moe_problem* p, const void* x, const void* Wg
                              const void* W1, const void* W3, const void* W2, const void* Ws1,
                              const void* Ws3, const void* Ws2, const void* residual, void* y,
                              void* ws, size_t ws_bytes, void* stream);
+
+/* Router logits and probabilities without the top-k: logits [T, E] fp32 in
+ * the router's fixed order (bias included, as moe_route computes them),
+ * probs [T, E] the softmax (may be NULL).  For expert-choice routing. */
+int moe_router_logits(const moe_problem* p, const void* x, const void* Wg, const float* bias,
+                      float* logits, float* probs, void* stream);
+
+/* Expert-choice routing, the selection (notes page, "Major Variants": each
+ * expert chooses its tokens).  From the router logits [T, E] of
+ * moe_router_logits and C = C_expert of moe_capacity (C <= T):
+ *   expert e takes the C tokens with the largest logits[t, e], equal values
+ *   in ascending token order (the choice is taken on the router's own fp32
+ *   values, so it is exact);
+ *   row_token[e*C + j]  = its j-th token in ascending token order  [E*C]
+ *   expert_offsets[e]   = e*C                                       [E+1]
+ *   sel_row[t*E + e]    = the row of (t, e), or -1 if e did not take t  [T*E]
+ * Exact (integer radix select and scans).  Needs p->flags to include
+ * MOE_FLAG_EXPERT_CHOICE.  No workspace. */
+int moe_expert_choice_assign(const moe_problem* p, const float* logits, int32_t* row_token,
+                             int32_t* expert_offsets, int32_t* sel_row, void* stream);
+
+/* Combine for expert-choice routing:
+ *   y[t] = ((sum over e with sel_row[t,e] >= 0, ascending e, of
+ *            probs[t,e] * yd[sel_row[t,e]]) + shared[t]) + residual[t]
+ * fp32 accumulation, one rounding; shared and residual may be NULL. */
+int moe_combine_expert_choice(const moe_problem* p, const void* yd, const float* probs,
+                              const int32_t* sel_row, const void* shared, const void* residual,
+                              void* y, void* stream);
 
 /* Slot assignment without a workspace, for callers that cannot allocate
  * device memory (an operator inside a host framework that owns every device

@@ -58,6 +58,7 @@ class Workload:
     zipf_s: Optional[float] = None  # skewed router bias; None = no bias
     renorm: bool = False            # renormalise the k gates of a token to sum to one
     ffn_shared: int = 0             # width of a shared expert every token goes through; 0 = none
+    expert_choice: bool = False     # experts take their tokens (instead of tokens their experts)
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
