@@ -45,8 +45,9 @@
 //            in, fp32 accumulate; each commit arrives on the barriers of both
 //            CTAs (stage free / tile done);
 //   warps 2-5 epilogue: tcgen05.ld of this CTA's accumulator rows (warp w
-//            reads TMEM lanes 32*(w%4)..+31), activation, bf16 round, masked
-//            stores of the rows that belong to the tile's expert; then both
+//            reads TMEM lanes 32*(w%4)..+31), activation, bf16 round, staged
+//            through shared memory and stored as 128-byte row segments, only
+//            the rows that belong to the tile's expert; then both
 //            CTAs' epilogue warps release the accumulator on the leader's
 //            barrier.
 // Every mbarrier wait is bounded in time; on expiry the kernel records
@@ -90,7 +91,15 @@ struct __align__(8) TcShared {
     int queue[kMaxE];              // experts whose down segments are not placed yet
     int queue_end[kMaxE];          // tile position where each one's gate/up segment ends
 };
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(TcShared);
+// Epilogue staging: each epilogue warp writes 64 output columns of its 32
+// rows into a padded shared buffer, then stores them four 128-byte row
+// segments per instruction (instead of 32 scattered 16-byte pieces).
+constexpr int kStgCols = 64;
+constexpr int kStgPitch = kStgCols * 2 + 16;  // bytes; rows 16 B apart in bank space
+constexpr int kStgWarpBytes = 32 * kStgPitch;
+constexpr size_t kStgOffset = (size_t)STAGES * STAGE_BYTES + ((sizeof(TcShared) + 127) / 128) * 128;
+constexpr size_t kSmemBytes = 1024 + kStgOffset + 4 * kStgWarpBytes;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct FfnArgs {
     int E, d, ffn, rows_max;
@@ -487,7 +496,6 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
     } else if (warp >= 2) {
         // --------------------------------------------------- epilogue --
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row_in_tile = q * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = cluster; tile < total_tiles; tile += nclusters) {
@@ -496,59 +504,61 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
             if (!wait_phase(smem_u32(&S.tfull[acc]), acc_phase, abort_flag, status)) break;
             tc_fence_after();
             const int rows_e = S.offs[e + 1] - S.offs[e];
-            const int local_row = mt * BM + row_in_tile;
-            const bool valid = local_row < rows_e;
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            if (kind == 0) {
-                // SwiGLU: columns 0-127 of the accumulator are gate, 128-255 up
-                const int n_out = args.ffn, col0 = nt * (BN / 2);
-                __nv_bfloat16* orow = args.h + (size_t)(S.offs[e] + local_row) * n_out;
+            uint8_t* stg = stages + kStgOffset + (size_t)q * kStgWarpBytes;
+            const int n_out = kind == 0 ? args.ffn : args.d;
+            const int ncols = kind == 0 ? BN / 2 : BN;  // output columns of this tile
+            const int col0 = nt * ncols;
+            __nv_bfloat16* obase =
+                (kind == 0 ? args.h : args.yd) + (size_t)(S.offs[e] + mt * BM + q * 32) * n_out;
+            const int rows_left = rows_e - (mt * BM + q * 32);  // this warp's rows [0, rows_left) are stored
 #pragma unroll 1
-                for (int c = 0; c < BN / 2; c += 16) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(taddr + c, g);
-                    tmem_ld16(taddr + BN / 2 + c, u);
-                    tmem_ld_wait();
+            for (int part = 0; part < ncols; part += kStgCols) {
+#pragma unroll 1
+                for (int c = 0; c < kStgCols; c += 16) {
                     uint32_t pk[8];
+                    if (kind == 0) {
+                        // SwiGLU: accumulator columns 0-127 are gate, 128-255 up
+                        uint32_t g[16], u[16];
+                        tmem_ld16(taddr + part + c, g);
+                        tmem_ld16(taddr + BN / 2 + part + c, u);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float h2[2];
+                        for (int j = 0; j < 8; ++j) {
+                            float h2[2];
 #pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            const float a = __uint_as_float(g[2 * j + z]);
-                            const float b = __uint_as_float(u[2 * j + z]);
-                            h2[z] = __fdividef(a, 1.0f + __expf(-a)) * b;
+                            for (int z = 0; z < 2; ++z) {
+                                const float a = __uint_as_float(g[2 * j + z]);
+                                const float b = __uint_as_float(u[2 * j + z]);
+                                h2[z] = __fdividef(a, 1.0f + __expf(-a)) * b;
+                            }
+                            pk[j] = pack_bf16x2(h2[0], h2[1]);
                         }
-                        pk[j] = pack_bf16x2(h2[0], h2[1]);
-                    }
-                    if (valid) {
+                    } else {
+                        uint32_t a[16];
+                        tmem_ld16(taddr + part + c, a);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 2; ++v)
-                            if (col0 + c + 8 * v < n_out)
-                                st_v16(orow + col0 + c + 8 * v,
-                                       Vec16{{pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]}});
+                        for (int j = 0; j < 8; ++j)
+                            pk[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
+                    }
+                    uint32_t* srow = reinterpret_cast<uint32_t*>(stg + lane * kStgPitch + c * 2);
+                    *reinterpret_cast<uint4*>(srow) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4*>(srow + 4) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+                __syncwarp();
+                // four rows of 128 B per instruction; rows past the expert and
+                // columns past n_out are not stored
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + (lane >> 3), ch = lane & 7;
+                    const int col = col0 + part + ch * 8;
+                    if (r < rows_left && col < n_out) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(stg + r * kStgPitch + ch * 16);
+                        st_v16(obase + (size_t)r * n_out + col, Vec16{{v.x, v.y, v.z, v.w}});
                     }
                 }
-            } else {
-                const int n_out = args.d, col0 = nt * BN;
-                __nv_bfloat16* orow = args.yd + (size_t)(S.offs[e] + local_row) * n_out;
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 16) {
-                    uint32_t a[16];
-                    tmem_ld16(taddr + c, a);
-                    tmem_ld_wait();
-                    uint32_t pk[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        pk[j] = pack_bf16x2(__uint_as_float(a[2 * j]), __uint_as_float(a[2 * j + 1]));
-                    if (valid) {
-#pragma unroll
-                        for (int v = 0; v < 2; ++v)
-                            if (col0 + c + 8 * v < n_out)
-                                st_v16(orow + col0 + c + 8 * v,
-                                       Vec16{{pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]}});
-                    }
-                }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();

@@ -16,18 +16,19 @@
 //
 // That order maps onto a warp: lane j owns slice j.  A CTA handles one
 // assignment block of 32 tokens with 8 warps; warp w owns tokens 4w..4w+3
-// and, in pass p, experts 8p..8p+7 -- 32 (token, expert) pairs, so each lane
-// keeps 32 slice sums and every 16-byte shared-memory load feeds 32 (x row) or
-// 64 (Wg row) multiply-adds per lane.  The hidden dimension is walked in
+// and, in pass p, experts RE*p..RE*p+RE-1 (RE = 8, or 16 for 9..64 experts) --
+// 4*RE (token, expert) pairs, so each lane keeps 4*RE slice sums and every
+// 16-byte shared-memory load feeds 8*RE (x row) or 32 (Wg row) multiply-adds
+// per lane.  The hidden dimension is walked in
 // chunks of 256 elements (8 per lane) through an S-stage ring of cp.async
 // copies (32 x rows and the pass's 8 Wg rows, in their storage type,
 // zero-filled past T, E and d; a zero element adds an exact zero product).
-// After the last chunk of a pass the warp reduces its 32 pairs with the
+// After the last chunk of a pass the warp reduces its pairs with the
 // butterfly in reduce-scatter form: in round o a lane keeps the half of its
 // pairs selected by bit o of its lane index and adds the partner's copy of
 // that half, which is the butterfly's own sum s[j] + s[j ^ o] for those pairs;
-// after five rounds lane j holds pair j.  Passes repeat for every group of 8
-// experts, re-reading x from L2.
+// after five rounds lane j holds pairs (4*RE/32) j .. (4*RE/32) j + 4*RE/32 - 1.
+// Passes repeat for every group of RE experts, re-reading x from L2.
 //
 // Softmax and top-k run from a shared-memory logit table: one thread per token
 // for up to 32 experts, one warp per token above that.  The gate of choice r
@@ -47,11 +48,9 @@ namespace moe {
 namespace {
 
 constexpr int kRT = 4;                       // tokens per warp tile
-constexpr int kRE = 8;                       // experts per warp tile (one pass)
 constexpr int kRouteThreads = 256;           // 8 warps x 4 tokens = 32 tokens
 constexpr int kTok = 32;                     // tokens per CTA
 constexpr int kKC = 256;                     // hidden elements per chunk (32 lanes x 8)
-constexpr int kStageRows = kTok + kRE;       // x rows, then the pass's Wg rows
 static_assert(kTok == kAssignBlock, "one CTA per assignment block");
 static_assert(kRouteThreads / 32 * kRT == kTok, "warp tiles cover the CTA's tokens");
 
@@ -77,8 +76,8 @@ __device__ __forceinline__ void load8(const uint8_t* p, float (&v)[8], float*) {
 
 // One reduce-scatter round of the butterfly over offset O: of the N values
 // a[0..N), keep the half chosen by bit O of the lane and add the partner's.
-template <int O, int N>
-__device__ __forceinline__ void rs_round(float (&a)[32], int lane) {
+template <int O, int N, int M>
+__device__ __forceinline__ void rs_round(float (&a)[M], int lane) {
     const bool hi = (lane & O) != 0;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {
@@ -106,13 +105,15 @@ __host__ __device__ constexpr int route_stages() {
     return sizeof(T) == 2 ? 4 : 3;
 }
 
+// experts per pass: 8, or 16 above 8 experts
+template <int RE>
 size_t route_smem_bytes(int elem_bytes, int stages, int E, int k) {
-    const int epad = (E + kRE - 1) / kRE * kRE;
-    return (size_t)stages * kStageRows * kKC * elem_bytes + (size_t)kTok * (epad + 1) * sizeof(float) +
+    const int epad = (E + RE - 1) / RE * RE;
+    return (size_t)stages * (kTok + RE) * kKC * elem_bytes + (size_t)kTok * (epad + 1) * sizeof(float) +
            (size_t)k * E * sizeof(int);
 }
 
-template <typename T>
+template <typename T, int RE>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
              const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
@@ -122,11 +123,14 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
     constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
     constexpr int VPR = RP / 16;                     // 16-byte vectors per ring row
+    constexpr int kStageRows = kTok + RE;            // x rows, then the pass's Wg rows
+    constexpr int NP = kRT * RE;                     // (token, expert) pairs per warp
+    constexpr int PL = NP / 32;                      // pairs per lane after the butterfly
 
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t* ring = smem;  // [S][kStageRows][RP]
-    const int npass = (E + kRE - 1) / kRE;
-    const int LGP = npass * kRE + 1;
+    const int npass = (E + RE - 1) / RE;
+    const int LGP = npass * RE + 1;
     float* lg = reinterpret_cast<float*>(smem + (size_t)S * kStageRows * RP);  // [kTok][LGP]
     int* cnt = reinterpret_cast<int*>(lg + kTok * LGP);                         // [k][E]
 
@@ -154,7 +158,7 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                     ok = in_d && t0 + row < T_;
                     src = x + (ok ? (size_t)(t0 + row) * d + k0 + col : 0);
                 } else {
-                    const int e = pass * kRE + row - kTok;
+                    const int e = pass * RE + row - kTok;
                     ok = in_d && e < E;
                     src = Wg + (ok ? (size_t)e * d + k0 + col : 0);
                 }
@@ -164,9 +168,9 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
         cp_async_commit();
     };
 
-    float acc[32];  // slice sums of pair p = rt * 8 + re
+    float acc[NP];  // slice sums of pair p = rt * RE + re
 #pragma unroll
-    for (int p = 0; p < 32; ++p) acc[p] = 0.0f;
+    for (int p = 0; p < NP; ++p) acc[p] = 0.0f;
 
 #pragma unroll
     for (int q = 0; q < S - 1; ++q) issue(q);
@@ -180,31 +184,36 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
 #pragma unroll
         for (int rt = 0; rt < kRT; ++rt) load8(base + (size_t)(kRT * warp + rt) * RP, xv[rt], (T*)nullptr);
 #pragma unroll
-        for (int re = 0; re < kRE; ++re) {
+        for (int re = 0; re < RE; ++re) {
             float wv[8];
             load8(base + (size_t)(kTok + re) * RP, wv, (T*)nullptr);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
 #pragma unroll
-                for (int rt = 0; rt < kRT; ++rt) acc[rt * kRE + re] = fmaf(xv[rt][j], wv[j], acc[rt * kRE + re]);
+                for (int rt = 0; rt < kRT; ++rt) acc[rt * RE + re] = fmaf(xv[rt][j], wv[j], acc[rt * RE + re]);
         }
         const int pass = q / nchunks;
         if (q - pass * nchunks == nchunks - 1) {
-            // end of a pass: butterfly in reduce-scatter form, lane j gets pair j
-            rs_round<16, 32>(acc, lane);
-            rs_round<8, 16>(acc, lane);
-            rs_round<4, 8>(acc, lane);
-            rs_round<2, 4>(acc, lane);
-            rs_round<1, 2>(acc, lane);
-            const int tl = kRT * warp + (lane >> 3);
-            const int e = pass * kRE + (lane & 7);
-            if (e < E) {
-                const float g = bias ? acc[0] + bias[e] : acc[0];
-                lg[tl * LGP + e] = g;
-                if (logits && t0 + tl < T_) logits[(size_t)(t0 + tl) * E + e] = g;
+            // end of a pass: butterfly in reduce-scatter form, lane j gets
+            // pairs PL*j .. PL*j + PL - 1
+            rs_round<16, NP>(acc, lane);
+            rs_round<8, NP / 2>(acc, lane);
+            rs_round<4, NP / 4>(acc, lane);
+            rs_round<2, NP / 8>(acc, lane);
+            rs_round<1, NP / 16>(acc, lane);
+#pragma unroll
+            for (int i = 0; i < PL; ++i) {
+                const int pr = PL * lane + i;
+                const int tl = kRT * warp + pr / RE;
+                const int e = pass * RE + pr % RE;
+                if (e < E) {
+                    const float g = bias ? acc[i] + bias[e] : acc[i];
+                    lg[tl * LGP + e] = g;
+                    if (logits && t0 + tl < T_) logits[(size_t)(t0 + tl) * E + e] = g;
+                }
             }
 #pragma unroll
-            for (int p = 0; p < 32; ++p) acc[p] = 0.0f;
+            for (int p = 0; p < NP; ++p) acc[p] = 0.0f;
         }
     }
     cp_async_wait<0>();
@@ -318,18 +327,29 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     }
 }
 
-template <typename T>
-cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
-                           int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
-                           const AssignScan& scan, cudaStream_t s) {
-    const size_t smem = route_smem_bytes((int)sizeof(T), route_stages<T>(), p.E, p.k);
-    auto kern = route_kernel<T>;
+template <typename T, int RE>
+cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, const float* bias,
+                            int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
+                            const AssignScan& scan, cudaStream_t s) {
+    const size_t smem = route_smem_bytes<RE>((int)sizeof(T), route_stages<T>(), p.E, p.k);
+    auto kern = route_kernel<T, RE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
     return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, p.T, p.d, p.E, p.k, (const T*)x,
                     (const T*)Wg, bias, topk_idx, topk_gate, probs, logits, (int)(p.flags & MOE_FLAG_RENORM),
                     scan);
+}
+
+// 16 experts per pass for 9..64 experts (measured faster at 64), 8 otherwise
+// (measured faster at 8 and 128)
+template <typename T>
+cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
+                           int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
+                           const AssignScan& scan, cudaStream_t s) {
+    if (p.E > 8 && p.E <= 64)
+        return launch_route_re<T, 16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, scan, s);
+    return launch_route_re<T, 8>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, scan, s);
 }
 
 }  // namespace
