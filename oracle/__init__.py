@@ -60,6 +60,7 @@ def _load():
         lib.oracle_router_logits.argtypes = [i64, i32, i32, i32, P, P, P, P]
         lib.oracle_softmax_topk.argtypes = [i64, i32, i32, i32, P, P, P, P]
         lib.oracle_assign.argtypes = [i64, i32, i32, i32, i64, i64] + [P] * 10
+        lib.oracle_assign_reroute.argtypes = [i64, i32, i32, i32, i64, i64] + [P] * 16
         lib.oracle_dispatch.argtypes = [i64, i32, i32, P, P, P]
         lib.oracle_expert_ffn.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P]
         lib.oracle_combine.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P, P, P]
@@ -165,6 +166,40 @@ def assign(topk_idx: np.ndarray, E: int, D: int, capacity_factor: float) -> Slot
                           ctypes.byref(dropped))
     return Slots(slot_pos, cr, ck, eo, so, sr, sov, row_token[: int(eo[E])].copy(),
                  dropped.value, C, Cs, rows_max)
+
+
+@dataclass
+class Rerouted(Slots):
+    route_idx: np.ndarray   # [T, k] expert that serves (t, r): the choice, or its fallback
+    route_gate: np.ndarray  # [T, k] weight of (t, r): that expert's gate
+    rerouted: int           # rerouted assignments that got a slot
+
+
+def assign_reroute(topk_idx: np.ndarray, topk_gate: np.ndarray, fallback_idx: np.ndarray,
+                   fallback_gate: np.ndarray, E: int, D: int, capacity_factor: float) -> Rerouted:
+    """Slot assignment where an overflowing choice goes once to the token's
+    next-best expert (fallback j for its j-th overflowing choice) and takes
+    the capacity the first pass left."""
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, k = idx.shape
+    gate = np.ascontiguousarray(topk_gate, dtype=np.float32)
+    fidx = np.ascontiguousarray(fallback_idx, dtype=np.int32)
+    fgate = np.ascontiguousarray(fallback_gate, dtype=np.float32)
+    assert gate.shape == fidx.shape == fgate.shape == (T, k)
+    C, Cs, rows_max = capacity(T, k, E, D, capacity_factor)
+    ridx, rgate = np.empty((T, k), np.int32), np.empty((T, k), np.float32)
+    slot_pos = np.empty((T, k), np.int32)
+    cr, ck = np.empty(E, np.int32), np.empty(E, np.int32)
+    eo, so = np.empty(E + 1, np.int32), np.empty(D + 1, np.int32)
+    sr, sov = np.empty(D, np.int32), np.empty(D, np.int32)
+    row_token = np.full(max(rows_max, 1), -1, np.int32)
+    rerouted, dropped = ctypes.c_int64(), ctypes.c_int64()
+    _load().oracle_assign_reroute(T, E, D, k, C, Cs, _ptr(idx), _ptr(gate), _ptr(fidx), _ptr(fgate),
+                                  _ptr(ridx), _ptr(rgate), _ptr(slot_pos), _ptr(cr), _ptr(ck), _ptr(eo),
+                                  _ptr(so), _ptr(sr), _ptr(sov), _ptr(row_token), ctypes.byref(rerouted),
+                                  ctypes.byref(dropped))
+    return Rerouted(slot_pos, cr, ck, eo, so, sr, sov, row_token[: int(eo[E])].copy(), dropped.value, C, Cs,
+                    rows_max, ridx, rgate, rerouted.value)
 
 
 def dispatch(x, row_token: np.ndarray) -> np.ndarray:
@@ -305,6 +340,14 @@ def route(x, Wg, bias, k: int, want_probs: bool = True, renorm: bool = False):
     g = router_logits(x, Wg, bias)
     probs, idx, gate = softmax_topk(g, k, want_probs, renorm)
     return g, probs, idx, gate
+
+
+def route_fallback(x, Wg, bias, k: int, want_probs: bool = True):
+    """Router with the k choices and the token's next k experts in the same
+    descending-logit order (its fallbacks), each with its softmax probability."""
+    g = router_logits(x, Wg, bias)
+    probs, idx2, gate2 = softmax_topk(g, 2 * k, want_probs)
+    return g, probs, idx2[:, :k].copy(), gate2[:, :k].copy(), idx2[:, k:].copy(), gate2[:, k:].copy()
 
 
 def layer_forward(x, Wg, bias, W1, W3, W2, k: int, D: int, capacity_factor: float,

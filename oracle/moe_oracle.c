@@ -37,6 +37,14 @@
  *   oracle_expert_ffn      pinned (dense soft-MoE / plain MLP special cases
  *                          against a library matmul)
  *   oracle_combine         pinned (dense all-experts brute force)
+ *   oracle_assign_reroute  pinned ([TI] worked example with its two dropped
+ *                          assignments rerouted by hand, invariants, no
+ *                          overflow = plain assignment)
+ *   oracle_routing_stats   pinned (closed forms: uniform, one-hot, hand
+ *                          example)
+ *   oracle_expert_choice   pinned (brute-force sort, ties, c = infinity)
+ *   oracle_combine_expert_choice  pinned (dense brute force when every
+ *                          expert takes every token)
  */
 #include <math.h>
 #include <stdint.h>
@@ -251,6 +259,105 @@ void oracle_assign(int64_t T, int E, int D, int k, int64_t C, int64_t C_shard,
             if (pos >= 0) row_token[expert_offsets[topk_idx[(size_t)t * k + r]] + pos] = (int32_t)t;
         }
     *dropped = ndrop;
+    free(cnt);
+}
+
+/* ------------------------------------------------------------------------ *
+ * Slot assignment with overflow rerouting.  [NG] "Capacity Factor and Token
+ * Dropping" and the load-imbalance list: tokens routed to a full expert are
+ * dropped or redirected to a secondary expert, the next-best one; [NG]
+ * "Components and Architecture": overflow tokens handled by a fallback
+ * routing.
+ *
+ * Readings (the pages name the fallback only):
+ *  - first pass: the plain assignment above on the k choices -- every
+ *    first choice keeps the slot it has without rerouting;
+ *  - the next-best expert of a token is the next one in its descending-logit
+ *    order after its k choices (fallback_idx[t, j] = its rank k + j expert,
+ *    fallback_gate[t, j] = that expert's softmax probability); the j-th
+ *    overflowing choice of token t (ascending rank) goes to fallback j, so a
+ *    token's experts stay distinct;
+ *  - rerouted assignments take the capacity the first pass left, in the same
+ *    priority order (rank r of the overflowing choice, then token):
+ *    pos = kept_first[e] + number of earlier rerouted assignments to e; kept
+ *    iff pos < C.  One level only: a rerouted assignment that finds its
+ *    fallback full is dropped;
+ *  - the assignment then counts for its fallback expert: route_idx[t, r] is
+ *    the expert that serves it, route_gate[t, r] its weight (the fallback's
+ *    probability when rerouted), slot_pos[t, r] its position or -1.
+ * counts_routed and the shard statistics describe the k choices (before
+ * capacity, as in the plain assignment); counts_kept, expert_offsets,
+ * shard_offsets and row_token describe the rows after rerouting;
+ * *rerouted = rerouted assignments that got a slot, *dropped = assignments
+ * with no slot at the end.
+ * ------------------------------------------------------------------------ */
+void oracle_assign_reroute(int64_t T, int E, int D, int k, int64_t C, int64_t C_shard,
+                           const int32_t* topk_idx, const float* topk_gate,
+                           const int32_t* fallback_idx, const float* fallback_gate,
+                           int32_t* route_idx, float* route_gate, int32_t* slot_pos,
+                           int32_t* counts_routed, int32_t* counts_kept,
+                           int32_t* expert_offsets, int32_t* shard_offsets,
+                           int32_t* shard_routed, int32_t* shard_overflow,
+                           int32_t* row_token, int64_t* rerouted, int64_t* dropped) {
+    int64_t* cnt = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t* fill = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t* first_pos = (int64_t*)malloc(sizeof(int64_t) * (size_t)(T * k > 0 ? T * k : 1));
+    /* first pass: the k choices in priority order */
+    for (int r = 0; r < k; ++r)
+        for (int64_t t = 0; t < T; ++t) first_pos[(size_t)t * k + r] = cnt[topk_idx[(size_t)t * k + r]]++;
+    for (int e = 0; e < E; ++e) fill[e] = cnt[e] < C ? cnt[e] : C;
+    /* second pass: overflowing choices go to their fallback, same order */
+    int64_t nre = 0, ndrop = 0;
+    for (int r = 0; r < k; ++r) {
+        for (int64_t t = 0; t < T; ++t) {
+            const size_t i = (size_t)t * k + r;
+            if (first_pos[i] < C) {
+                route_idx[i] = topk_idx[i];
+                route_gate[i] = topk_gate[i];
+                slot_pos[i] = (int32_t)first_pos[i];
+                continue;
+            }
+            int j = 0; /* overflowing choices of t ranked before r */
+            for (int q = 0; q < r; ++q) j += first_pos[(size_t)t * k + q] >= C;
+            const int e = fallback_idx[(size_t)t * k + j];
+            route_idx[i] = e;
+            route_gate[i] = fallback_gate[(size_t)t * k + j];
+            const int64_t pos = fill[e]++;
+            if (pos < C) {
+                slot_pos[i] = (int32_t)pos;
+                ++nre;
+            } else {
+                slot_pos[i] = -1;
+                ++ndrop;
+            }
+        }
+    }
+    int64_t off = 0;
+    for (int e = 0; e < E; ++e) {
+        counts_routed[e] = (int32_t)cnt[e];
+        counts_kept[e] = (int32_t)(fill[e] < C ? fill[e] : C);
+        expert_offsets[e] = (int32_t)off;
+        off += counts_kept[e];
+    }
+    expert_offsets[E] = (int32_t)off;
+    int per = E / D;
+    for (int s = 0; s < D; ++s) {
+        int64_t routed = 0;
+        for (int e = s * per; e < (s + 1) * per; ++e) routed += cnt[e];
+        shard_routed[s] = (int32_t)routed;
+        shard_overflow[s] = (int32_t)(routed > C_shard ? routed - C_shard : 0);
+        shard_offsets[s] = expert_offsets[s * per];
+    }
+    shard_offsets[D] = expert_offsets[E];
+    for (int64_t t = 0; t < T; ++t)
+        for (int r = 0; r < k; ++r) {
+            const size_t i = (size_t)t * k + r;
+            if (slot_pos[i] >= 0) row_token[expert_offsets[route_idx[i]] + slot_pos[i]] = (int32_t)t;
+        }
+    *rerouted = nre;
+    *dropped = ndrop;
+    free(first_pos);
+    free(fill);
     free(cnt);
 }
 

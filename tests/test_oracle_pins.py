@@ -605,3 +605,127 @@ def test_expert_choice_with_every_token_is_the_dense_soft_mixture():
     ye = torch.einsum("tef,edf->ted", torch.nn.functional.silu(a) * u, W2.double())
     want = torch.einsum("te,ted->td", torch.from_numpy(probs).double(), ye)
     np.testing.assert_allclose(y, want.numpy(), rtol=1e-9, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# overflow rerouting to the next-best expert
+# --------------------------------------------------------------------------
+def _reroute_inputs(g, k):
+    probs, idx2, gate2 = oracle.softmax_topk(g, 2 * k)
+    return probs, idx2[:, :k], gate2[:, :k], idx2[:, k:], gate2[:, k:]
+
+
+def test_reroute_worked_example():
+    _, choices, _ = _worked_example()
+    rows = read_golden("worked_example_reroute.txt")
+    kv = {r[0]: r[1:] for r in rows if r[0] not in ("fallback", "rerouted")}
+    fallbacks = [tuple(int(v) for v in r[2:4]) for r in rows if r[0] == "fallback"]
+    moved = [tuple(int(v) for v in r[1:5]) for r in rows if r[0] == "rerouted"]
+    E, k = 8, 2
+    g = np.zeros((6, E), np.float32)
+    for t, e0, e1 in choices:
+        g[t, e0], g[t, e1] = 3.0, 2.0
+    probs, idx, gate, fidx, fgate = _reroute_inputs(g, k)
+    assert [tuple(r) for r in fidx.tolist()] == fallbacks
+    s = oracle.assign_reroute(idx, gate, fidx, fgate, E, 4, 1.0)
+    ints = lambda key: [int(v) for v in kv[key]]
+    assert s.counts_routed.tolist() == ints("counts_routed")
+    assert s.counts_kept.tolist() == ints("counts_kept")
+    assert s.expert_offsets.tolist() == ints("expert_offsets")
+    assert s.shard_offsets.tolist() == ints("shard_offsets")
+    assert s.shard_routed.tolist() == ints("shard_routed")
+    assert s.shard_overflow.tolist() == ints("shard_overflow")
+    assert s.row_token.tolist() == ints("row_token")
+    assert s.dropped == ints("dropped_after")[0] and s.rerouted == len(moved) == 2
+    S = math.exp(3) + math.exp(2) + 6
+    for t, r, e, pos in moved:
+        assert (s.route_idx[t, r], s.slot_pos[t, r]) == (e, pos)
+        assert abs(s.route_gate[t, r] - 1 / S) < 1e-8
+    # every other assignment keeps its choice, gate and first-pass position
+    plain = oracle.assign(idx, E, 4, 1.0)
+    for t in range(6):
+        for r in range(k):
+            if (t, r) not in [(m[0], m[1]) for m in moved]:
+                assert s.route_idx[t, r] == idx[t, r] and s.route_gate[t, r] == gate[t, r]
+                assert s.slot_pos[t, r] == plain.slot_pos[t, r] >= 0
+
+
+def _reroute_by_sorting(idx, fidx, E, C):
+    """The second pass restated as a sort: every overflowing choice, ordered
+    by (rank, token), bids for its fallback; expert e serves the first
+    C - kept_first[e] bids it receives."""
+    T, k = idx.shape
+    # first-pass position by a literal sort of all (expert, rank, token)
+    order = sorted(((int(idx[t, r]), r, t) for t in range(T) for r in range(k)))
+    pos1, last, n = {}, None, 0
+    for e, r, t in order:
+        n = n + 1 if e == last else 0
+        last = e
+        pos1[(t, r)] = n
+    kept_first = np.zeros(E, np.int64)
+    for (t, r), p in pos1.items():
+        kept_first[idx[t, r]] += p < C
+    bids = sorted((r, t) for (t, r), p in pos1.items() if p >= C)
+    served = {e: [] for e in range(E)}
+    target = {}
+    for r, t in bids:
+        j = sum(pos1[(t, q)] >= C for q in range(r))
+        e = int(fidx[t, j])
+        target[(t, r)] = e
+        served[e].append((t, r))
+    slot = {}
+    for e, lst in served.items():
+        for i, tr in enumerate(lst):
+            slot[tr] = kept_first[e] + i if kept_first[e] + i < C else -1
+    return pos1, target, slot
+
+
+@pytest.mark.parametrize("T,E,k,c,skew", [(300, 16, 2, 1.0, 2.0), (257, 8, 1, 0.5, 1.0),
+                                          (190, 32, 4, 1.25, 3.0), (64, 4, 2, 0.3, 0.0)])
+def test_reroute_against_sorting_and_invariants(T, E, k, c, skew):
+    rng = np.random.default_rng(T + E)
+    g = (rng.standard_normal((T, E)) + skew * np.log1p(np.arange(E))[None, ::-1]).astype(np.float32)
+    probs, idx, gate, fidx, fgate = _reroute_inputs(g, k)
+    s = oracle.assign_reroute(idx, gate, fidx, fgate, E, 2 if E % 2 == 0 else 1, c)
+    plain = oracle.assign(idx, E, 2 if E % 2 == 0 else 1, c)
+    C = s.C
+    pos1, target, slot = _reroute_by_sorting(idx, fidx, E, C)
+    n_moved = 0
+    for t in range(T):
+        assert len(set(s.route_idx[t].tolist())) == k  # a token's experts stay distinct
+        for r in range(k):
+            if pos1[(t, r)] < C:
+                assert s.route_idx[t, r] == idx[t, r] and s.slot_pos[t, r] == pos1[(t, r)]
+                assert s.route_gate[t, r] == gate[t, r]
+            else:
+                e = target[(t, r)]
+                j = list(fidx[t]).index(e)
+                assert s.route_idx[t, r] == e and s.route_gate[t, r] == fgate[t, j] == probs[t, e]
+                assert s.slot_pos[t, r] == slot[(t, r)]
+                if slot[(t, r)] < 0:
+                    assert s.counts_kept[e] == C  # dropped only when the fallback is full
+                else:
+                    n_moved += 1
+    assert s.rerouted == n_moved and s.rerouted + s.dropped == plain.dropped
+    assert (s.counts_kept <= C).all() and (s.counts_kept >= plain.counts_kept).all()
+    assert np.array_equal(s.counts_routed, plain.counts_routed)
+    assert np.array_equal(s.expert_offsets, np.concatenate([[0], np.cumsum(s.counts_kept)]))
+    for t in range(T):
+        for r in range(k):
+            if s.slot_pos[t, r] >= 0:
+                assert s.row_token[s.expert_offsets[s.route_idx[t, r]] + s.slot_pos[t, r]] == t
+    if skew > 0:
+        assert plain.dropped > 0 and s.rerouted > 0  # the cases do exercise the second pass
+
+
+def test_reroute_without_overflow_is_the_plain_assignment():
+    rng = np.random.default_rng(5)
+    g = rng.standard_normal((200, 8)).astype(np.float32)
+    _, idx, gate, fidx, fgate = _reroute_inputs(g, 2)
+    for c in (math.inf, 8.0):
+        s = oracle.assign_reroute(idx, gate, fidx, fgate, 8, 4, c)
+        p = oracle.assign(idx, 8, 4, c)
+        assert p.dropped == 0 and s.rerouted == 0 and s.dropped == 0
+        assert np.array_equal(s.route_idx, idx) and np.array_equal(s.route_gate, gate)
+        for f in ("slot_pos", "counts_routed", "counts_kept", "expert_offsets", "shard_offsets", "row_token"):
+            assert np.array_equal(getattr(s, f), getattr(p, f)), f
