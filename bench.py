@@ -305,32 +305,47 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError("device status after the shared-expert loop")
         del sin, sws, ys
 
+    def time_layer_variant(vwl, what):
+        """One whole moe_layer_forward of a layer variant per graph replay;
+        returns (mean ms, the variant's workspace)."""
+        vp = moe.problem_of(vwl)
+        vws = moe.alloc_workspace(vp, dev)
+        fn = lambda: moe.moe_layer_forward(vp, inp.x, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y, vws,
+                                           vws.numel(), None)
+        fn()
+        torch.cuda.synchronize(dev)
+        g_v = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_v):
+            fn()
+        v_ev = []
+        for _ in range(args.steps):
+            flush()
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            g_v.replay()
+            b_ev.record(stream)
+            v_ev.append((a_ev, b_ev))
+        torch.cuda.synchronize(dev)
+        if moe.moe_device_status(vws, stream) != moe.MOE_OK:
+            raise RuntimeError(f"device status after the {what} loop")
+        return statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in v_ev), vws
+
     # ---- the same layer with expert-choice routing (each expert takes its
-    # C highest-scoring tokens), one whole moe_layer_forward per replay
+    # C highest-scoring tokens)
     ewl = wl.with_(expert_choice=True)
-    ep = moe.problem_of(ewl)
-    ews = moe.alloc_workspace(ep, dev)
-    ec_fn = lambda: moe.moe_layer_forward(ep, inp.x, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y, ews,
-                                          ews.numel(), None)
-    ec_fn()
-    torch.cuda.synchronize(dev)
-    g_ec = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_ec):
-        ec_fn()
-    ec_ev = []
-    for _ in range(args.steps):
-        flush()
-        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a_ev.record(stream)
-        g_ec.replay()
-        b_ev.record(stream)
-        ec_ev.append((a_ev, b_ev))
-    torch.cuda.synchronize(dev)
-    ec_ms = statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in ec_ev)
-    if moe.moe_device_status(ews, stream) != moe.MOE_OK:
-        raise RuntimeError("device status after the expert-choice loop")
-    ec_rows = ewl.E * moe.moe_capacity(ep)[0]
+    ec_ms, ews = time_layer_variant(ewl, "expert-choice")
+    ec_rows = ewl.E * moe.moe_capacity(moe.problem_of(ewl))[0]
     del ews
+
+    # ---- the same layer with overflow rerouting to the next-best expert
+    rr_ms, rr_stats = None, None
+    if 2 * wl.k <= wl.E:
+        rwl = wl.with_(reroute=True)
+        rr_ms, rws = time_layer_variant(rwl, "rerouting")
+        rp = moe.problem_of(rwl)
+        rr_stats = {n: int(moe.workspace_view(rws, rp, n, torch.int32, 1).item()) for n in ("rerouted", "dropped")}
+        rr_stats["kept"] = int(moe.workspace_view(rws, rp, "expert_offsets", torch.int32, wl.E + 1)[-1].item())
+        del rws
 
     # ---- end to end through moe_layer_forward with host buffers
     x_host = inp.x.cpu().pin_memory()
@@ -389,6 +404,9 @@ def run_ours(args, rank, world, local_rank):
                 "frac_bf16": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / (bf16_tf * 1e12)},
             "expert_choice_layer": {"ms": ec_ms, "tokens_per_s": wl.T / (ec_ms * 1e-3), "rows": ec_rows,
                                     "note": "whole moe_layer_forward with expert-choice routing, graph replay"},
+            "reroute_layer": None if rr_ms is None else dict(
+                ms=rr_ms, tokens_per_s=wl.T / (rr_ms * 1e-3), **rr_stats,
+                note="whole moe_layer_forward with overflow rerouting, graph replay"),
             "routing_stats": {"ms": stats_ms, "GB_s": gb(wl.T * wl.E * 4 + 8 * wl.E, stats_ms),
                               "aux": stats_vals[0], "entropy": stats_vals[1], "drop": stats_vals[2],
                               "imbalance": stats_vals[3]},

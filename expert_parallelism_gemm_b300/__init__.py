@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_F32, MOE_BF16 = 0, 1
-MOE_FLAG_RENORM, MOE_FLAG_EXPERT_CHOICE = 1, 2
+MOE_FLAG_RENORM, MOE_FLAG_EXPERT_CHOICE, MOE_FLAG_REROUTE = 1, 2, 4
 MOE_ACT_SWIGLU, MOE_ACT_GELU = 0, 1
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
@@ -32,7 +32,8 @@ EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe
            "moe_layer_forward", "moe_device_status", "moe_status_string",
            "moe_assign_slots_static", "moe_routing_stats", "moe_shared_expert_ffn",
            "moe_combine_shared", "moe_layer_forward_shared", "moe_expert_choice_assign",
-           "moe_combine_expert_choice", "moe_router_logits")
+           "moe_combine_expert_choice", "moe_router_logits", "moe_route_fallback",
+           "moe_assign_slots_reroute")
 
 
 class moe_problem(ctypes.Structure):
@@ -45,7 +46,7 @@ class moe_problem(ctypes.Structure):
 _LAYOUT_FIELDS = ("status", "topk_idx", "topk_gate", "slot_pos", "counts_routed", "counts_kept",
                   "expert_offsets", "shard_offsets", "shard_routed", "shard_overflow", "dropped",
                   "hist", "row_token", "xd", "h", "yd", "ffn_sync", "stats", "hs", "ys", "shared_sync",
-                  "probs", "logits", "sel_row", "total")
+                  "probs", "logits", "sel_row", "fallback_idx", "fallback_gate", "rerouted", "total")
 
 
 class moe_workspace_layout(ctypes.Structure):
@@ -91,6 +92,8 @@ def load() -> ctypes.CDLL:
     lib.moe_expert_choice_assign.argtypes = [PP, P, P, P, P, P]
     lib.moe_router_logits.argtypes = [PP, P, P, P, P, P, P]
     lib.moe_combine_expert_choice.argtypes = [PP, P, P, P, P, P, P, P]
+    lib.moe_route_fallback.argtypes = [PP] + [P] * 9
+    lib.moe_assign_slots_reroute.argtypes = [PP] + [P] * 17 + [sz, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for n in EXPORTS:
@@ -124,22 +127,23 @@ def _check(rc: int, where: str):
 
 
 def make_problem(T, d, E, D, k, ffn, capacity_factor, dtype="bf16", act="swiglu", renorm=False,
-                 ffn_shared=0, expert_choice=False) -> moe_problem:
+                 ffn_shared=0, expert_choice=False, reroute=False) -> moe_problem:
     """moe_problem from plain values; dtype 'bf16'|'f32' (or code), act 'swiglu'|'gelu'."""
     dt = {"bf16": MOE_BF16, "f32": MOE_F32}.get(dtype, dtype)
     ac = {"swiglu": MOE_ACT_SWIGLU, "gelu": MOE_ACT_GELU}.get(act, act)
     return moe_problem(int(T), int(d), int(E), int(D), int(k), int(ffn), float(capacity_factor),
                        int(dt), int(ac),
-                       (MOE_FLAG_RENORM if renorm else 0) | (MOE_FLAG_EXPERT_CHOICE if expert_choice else 0),
+                       (MOE_FLAG_RENORM if renorm else 0) | (MOE_FLAG_EXPERT_CHOICE if expert_choice else 0)
+                       | (MOE_FLAG_REROUTE if reroute else 0),
                        int(ffn_shared))
 
 
 def problem_of(wl) -> moe_problem:
     """moe_problem from any object with T, d, E, D, k, ffn, capacity_factor, dtype, act
-    (and optionally renorm, ffn_shared)."""
+    (and optionally renorm, ffn_shared, expert_choice, reroute)."""
     return make_problem(wl.T, wl.d, wl.E, wl.D, wl.k, wl.ffn, wl.capacity_factor, wl.dtype, wl.act,
                         getattr(wl, "renorm", False), getattr(wl, "ffn_shared", 0),
-                        getattr(wl, "expert_choice", False))
+                        getattr(wl, "expert_choice", False), getattr(wl, "reroute", False))
 
 
 # -------------------------------------------------------------- entries --
@@ -181,6 +185,28 @@ def moe_assign_slots(problem, topk_idx, slot_pos, counts_routed, counts_kept, ex
                                    _p(row_token), _p(dropped), _p(ws), int(ws_bytes),
                                    _stream(stream)),
            "moe_assign_slots")
+
+
+def moe_route_fallback(problem, x, Wg, bias, topk_idx, topk_gate, fallback_idx, fallback_gate, probs,
+                       stream=None):
+    _check(load().moe_route_fallback(ctypes.byref(problem), _p(x), _p(Wg), _p(bias), _p(topk_idx),
+                                     _p(topk_gate), _p(fallback_idx), _p(fallback_gate), _p(probs),
+                                     _stream(stream)),
+           "moe_route_fallback")
+
+
+def moe_assign_slots_reroute(problem, topk_idx, topk_gate, fallback_idx, fallback_gate, route_idx,
+                             route_gate, slot_pos, counts_routed, counts_kept, expert_offsets, shard_offsets,
+                             shard_routed, shard_overflow, row_token, dropped, rerouted, ws, ws_bytes,
+                             stream=None):
+    _check(load().moe_assign_slots_reroute(ctypes.byref(problem), _p(topk_idx), _p(topk_gate),
+                                           _p(fallback_idx), _p(fallback_gate), _p(route_idx),
+                                           _p(route_gate), _p(slot_pos), _p(counts_routed),
+                                           _p(counts_kept), _p(expert_offsets), _p(shard_offsets),
+                                           _p(shard_routed), _p(shard_overflow), _p(row_token),
+                                           _p(dropped), _p(rerouted), _p(ws), int(ws_bytes),
+                                           _stream(stream)),
+           "moe_assign_slots_reroute")
 
 
 def moe_assign_slots_static(problem, topk_idx, slot_pos, counts_routed, counts_kept, expert_offsets,

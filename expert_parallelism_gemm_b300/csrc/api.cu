@@ -40,8 +40,12 @@ int validate(const moe_problem* p) {
     if (!(p->capacity_factor > 0.0)) return MOE_ERR_INVALID_ARG;  // also rejects NaN
     if (p->dtype != MOE_F32 && p->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
     if (p->act != MOE_ACT_SWIGLU && p->act != MOE_ACT_GELU) return MOE_ERR_INVALID_ARG;
-    if (p->flags & ~(MOE_FLAG_RENORM | MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
+    if (p->flags & ~(MOE_FLAG_RENORM | MOE_FLAG_EXPERT_CHOICE | MOE_FLAG_REROUTE)) return MOE_ERR_INVALID_ARG;
     if ((p->flags & MOE_FLAG_RENORM) && (p->flags & MOE_FLAG_EXPERT_CHOICE)) return MOE_ERR_INVALID_ARG;
+    // rerouting: plain probabilities as gates, top-k routing, k fallbacks per token
+    if ((p->flags & MOE_FLAG_REROUTE) && (p->flags & (MOE_FLAG_RENORM | MOE_FLAG_EXPERT_CHOICE)))
+        return MOE_ERR_INVALID_ARG;
+    if ((p->flags & MOE_FLAG_REROUTE) && 2 * p->k > p->E) return MOE_ERR_INVALID_ARG;
     if (p->ffn_shared < 0 || p->ffn_shared % 8) return MOE_ERR_INVALID_ARG;
     if (p->E > 256 || p->k > 8) return MOE_ERR_UNSUPPORTED;
     if (p->T * (int64_t)p->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
@@ -119,6 +123,10 @@ void layout(const Problem& p, moe_workspace_layout* L) {
     L->probs = take(TE * sizeof(float));
     L->logits = take(TE * sizeof(float));
     L->sel_row = take(TE * sizeof(int32_t));
+    const size_t Tkr = (p.flags & MOE_FLAG_REROUTE) ? Tk : 0;
+    L->fallback_idx = take(Tkr * 4);
+    L->fallback_gate = take(Tkr * 4);
+    L->rerouted = take(4);
     L->total = o;
 }
 
@@ -191,8 +199,21 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
                               (int32_t*)(w + L.shard_offsets), (int32_t*)(w + L.shard_routed),
                               (int32_t*)(w + L.shard_overflow), (int32_t*)(w + L.dropped),
                               (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C, p.C_shard};
-        e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
-        if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
+        if (p.flags & MOE_FLAG_REROUTE) {
+            // the choices and their fallbacks, then the reroute and place passes
+            // (final experts and gates overwrite idx and gate in place)
+            int32_t* fb_idx = (int32_t*)(w + L.fallback_idx);
+            float* fb_gate = (float*)(w + L.fallback_gate);
+            e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s, fb_idx, fb_gate);
+            AssignScan second = scan;
+            second.second = true;
+            second.rerouted = (int32_t*)(w + L.rerouted);
+            if (e == cudaSuccess)
+                e = launch_reroute(p, idx, gate, fb_idx, fb_gate, idx, gate, slot, second, row_token, status, s);
+        } else {
+            e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
+            if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
+        }
     }
     if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
     if (e == cudaSuccess) {
@@ -267,6 +288,7 @@ int moe_assign_slots(const moe_problem* mp, const int32_t* topk_idx, int32_t* sl
     Problem p;
     int rc = to_problem(mp, &p);
     if (rc != MOE_OK) return rc;
+    if (p.flags & MOE_FLAG_REROUTE) return MOE_ERR_INVALID_ARG;  // see moe_assign_slots_reroute
     if ((p.T > 0 && (!topk_idx || !slot_pos || !row_token)) || !counts_routed || !counts_kept ||
         !expert_offsets || !shard_offsets || !shard_routed || !shard_overflow)
         return MOE_ERR_INVALID_ARG;
@@ -277,6 +299,57 @@ int moe_assign_slots(const moe_problem* mp, const int32_t* topk_idx, int32_t* sl
     return cuda_rc(launch_assign(p, topk_idx, slot_pos, counts_routed, counts_kept, expert_offsets, shard_offsets,
                                  shard_routed, shard_overflow, row_token, dropped,
                                  (int32_t*)((char*)ws + L.hist), status, (cudaStream_t)stream));
+}
+
+int moe_route_fallback(const moe_problem* mp, const void* x, const void* Wg, const float* bias, int32_t* topk_idx,
+                       float* topk_gate, int32_t* fallback_idx, float* fallback_gate, float* probs, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!(p.flags & MOE_FLAG_REROUTE)) return MOE_ERR_INVALID_ARG;
+    if (p.T == 0) return MOE_OK;
+    if (!x || !Wg || !topk_idx || !topk_gate || !fallback_idx || !fallback_gate || !aligned16(x) ||
+        !aligned16(Wg))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_rc(launch_route(p, x, Wg, bias, topk_idx, topk_gate, probs, (cudaStream_t)stream, nullptr,
+                                fallback_idx, fallback_gate));
+}
+
+int moe_assign_slots_reroute(const moe_problem* mp, const int32_t* topk_idx, const float* topk_gate,
+                             const int32_t* fallback_idx, const float* fallback_gate, int32_t* route_idx,
+                             float* route_gate, int32_t* slot_pos, int32_t* counts_routed, int32_t* counts_kept,
+                             int32_t* expert_offsets, int32_t* shard_offsets, int32_t* shard_routed,
+                             int32_t* shard_overflow, int32_t* row_token, int32_t* dropped, int32_t* rerouted,
+                             void* ws, size_t ws_bytes, void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (!(p.flags & MOE_FLAG_REROUTE)) return MOE_ERR_INVALID_ARG;
+    if ((p.T > 0 && (!topk_idx || !topk_gate || !fallback_idx || !fallback_gate || !route_idx || !route_gate ||
+                     !slot_pos || !row_token)) ||
+        !counts_routed || !counts_kept || !expert_offsets || !shard_offsets || !shard_routed || !shard_overflow)
+        return MOE_ERR_INVALID_ARG;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    char* w = (char*)ws;
+    int* status = (int*)(w + L.status);
+    int32_t* hist = (int32_t*)(w + L.hist);
+    cudaStream_t s = (cudaStream_t)stream;
+    // first pass: count and scan of the k choices (no rank pass); T = 0 stops here with zero counts
+    const AssignScan first{hist, counts_routed, counts_kept, expert_offsets, shard_offsets, shard_routed,
+                           shard_overflow, dropped, (unsigned*)(status + 1), p.E, p.D, p.k, p.nblk, p.C,
+                           p.C_shard};
+    cudaError_t e = launch_count(p, topk_idx, first, status, s);
+    if (e != cudaSuccess || p.nblk == 0) {
+        if (e == cudaSuccess && rerouted) e = cudaMemsetAsync(rerouted, 0, sizeof(int32_t), s);
+        return cuda_rc(e);
+    }
+    AssignScan second = first;
+    second.second = true;
+    second.rerouted = rerouted;
+    return cuda_rc(launch_reroute(p, topk_idx, topk_gate, fallback_idx, fallback_gate, route_idx, route_gate,
+                                  slot_pos, second, row_token, status, s));
 }
 
 int moe_dispatch(const moe_problem* mp, const void* x, const int32_t* row_token, const int32_t* expert_offsets,

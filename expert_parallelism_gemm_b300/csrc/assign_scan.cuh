@@ -16,6 +16,12 @@
 // token -- and writes the routed and kept counts, expert and shard offsets,
 // shard statistics and the dropped total.  Integer arithmetic only, so the
 // result does not depend on which CTA finishes last.
+//
+// Second pass of overflow rerouting (`second` set): hist holds the counts of
+// the rerouted assignments; each expert's prefixes start from its first-pass
+// kept count (read from counts_kept), kept becomes min(first-pass kept +
+// rerouted, C), counts_routed is left as the first pass wrote it, and
+// `rerouted` receives the number of rerouted assignments that found room.
 #pragma once
 
 #include "common.cuh"
@@ -34,6 +40,8 @@ struct AssignScan {
     unsigned* ticket;  // zero before the launch; reset to zero by the last CTA
     int E, D, k;
     int64_t nblk, C, C_shard;
+    int32_t* rerouted = nullptr;  // second pass only; may be null
+    bool second = false;
 };
 
 // Call from every thread of every CTA after the CTA's hist entries are
@@ -43,6 +51,7 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
     __shared__ bool s_last;
     __shared__ int s_routed[256];
     __shared__ int s_kept_off[257];
+    __shared__ int s_moved[256];
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0)
@@ -56,7 +65,8 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
     // 256 entries per round (8 contiguous per lane, loads issued together)
     for (int e = warp; e < a.E; e += nwarps) {
         int32_t* h = a.hist + (size_t)e * L;
-        int running = 0;
+        const int first_kept = a.second ? __ldcg(a.counts_kept + e) : 0;
+        int running = first_kept;
         for (int64_t base = 0; base < L; base += 256) {
             const int64_t i0 = base + 8 * lane;
             int v[8];
@@ -81,9 +91,11 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
         }
         if (lane == 0) {
             const int kept = (int)min((int64_t)running, a.C);
-            s_routed[e] = running;
+            const int routed = a.second ? __ldcg(a.counts_routed + e) : running;
+            s_routed[e] = routed;
             s_kept_off[e] = kept;
-            a.counts_routed[e] = running;
+            s_moved[e] = kept - first_kept;
+            if (!a.second) a.counts_routed[e] = routed;
             a.counts_kept[e] = kept;
         }
     }
@@ -91,20 +103,22 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
     if (warp == 0) {
         // expert offsets: exclusive scan of the kept counts (E <= 256)
         const int per = (a.E + 31) / 32;
-        int loc_kept = 0, loc_drop = 0;
+        int loc_kept = 0, loc_drop = 0, loc_moved = 0;
         for (int j = 0; j < per; ++j) {
             const int e = lane * per + j;
             if (e < a.E) {
                 loc_kept += s_kept_off[e];
                 loc_drop += s_routed[e] - s_kept_off[e];
+                loc_moved += s_moved[e];
             }
         }
-        int incl = loc_kept, drop = loc_drop;
+        int incl = loc_kept, drop = loc_drop, moved = loc_moved;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int n = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += n;
             drop += __shfl_xor_sync(0xffffffffu, drop, o);
+            moved += __shfl_xor_sync(0xffffffffu, moved, o);
         }
         int run = incl - loc_kept;
         for (int j = 0; j < per; ++j) {
@@ -122,6 +136,7 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
         }
         if (lane == 0) {
             if (a.dropped) a.dropped[0] = drop;
+            if (a.second && a.rerouted) a.rerouted[0] = moved;
             *a.ticket = 0u;  // ready for the next call on this scratch
         }
     }

@@ -67,6 +67,7 @@ extern "C" int moe_assign_slots_static(const moe_problem* mp, const int32_t* top
     Problem p;
     int rc = moe_capacity(mp, &p.C, &p.C_shard, &p.rows_max);  // validates the problem
     if (rc != MOE_OK) return rc;
+    if (mp->flags & MOE_FLAG_REROUTE) return MOE_ERR_INVALID_ARG;  // rerouting has its own entry point
     p.T = mp->T;
     p.d = mp->d;
     p.E = mp->E;

@@ -134,20 +134,37 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 // logits (optional): the fp32 router logits [T, E], bias included
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
                          int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s,
-                         float* logits = nullptr);
+                         float* logits = nullptr, int32_t* fallback_idx = nullptr,
+                         float* fallback_gate = nullptr);
 
 // router plus the count pass of the slot assignment (hist and scan outputs in
 // `scan`, defined in assign_scan.cuh); T must be > 0
 struct AssignScan;
+// fallback_idx / fallback_gate (optional, [T, k]): the token's next k experts
+// after its choices (ranks k .. 2k-1) and their probabilities
 cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
                                int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
-                               cudaStream_t s);
+                               cudaStream_t s, int32_t* fallback_idx = nullptr,
+                               float* fallback_gate = nullptr);
 
 cudaError_t launch_assign(const Problem& p, const int32_t* topk_idx, int32_t* slot_pos,
                           int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
                           int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
                           int32_t* row_token, int32_t* dropped, int32_t* hist, int* status,
                           cudaStream_t s);
+
+// count pass alone (histogram, then the last CTA's scan into a's outputs)
+cudaError_t launch_count(const Problem& p, const int32_t* topk_idx, const AssignScan& a, int* status,
+                         cudaStream_t s);
+
+// overflow rerouting after a count pass of the k choices (hist holds their
+// scanned prefixes): the reroute pass (with the second scan, `second` =
+// the same scan outputs with .second set) and the place pass.  route_idx /
+// route_gate may alias topk_idx / topk_gate.
+cudaError_t launch_reroute(const Problem& p, const int32_t* topk_idx, const float* topk_gate,
+                           const int32_t* fallback_idx, const float* fallback_gate, int32_t* route_idx,
+                           float* route_gate, int32_t* slot_pos, const AssignScan& second, int32_t* row_token,
+                           int* status, cudaStream_t s);
 
 // rank pass alone (the histogram already holds the scanned prefixes)
 cudaError_t launch_rank(const Problem& p, const int32_t* topk_idx, const int32_t* hist,

@@ -501,7 +501,11 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
         for (int tile = cluster; tile < total_tiles; tile += nclusters) {
             int kind, e, mt, nt, mp;
             tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
-            if (!wait_phase(smem_u32(&S.tfull[acc]), acc_phase, abort_flag, status)) break;
+            // every lane polls; the warp goes on only if all saw the tile done
+            // (tcgen05.ld below needs the whole warp), so an abort that races
+            // the phase cannot split it
+            if (!__all_sync(0xffffffffu, wait_phase(smem_u32(&S.tfull[acc]), acc_phase, abort_flag, status)))
+                break;
             tc_fence_after();
             const int rows_e = S.offs[e + 1] - S.offs[e];
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);

@@ -33,7 +33,9 @@
 // Softmax and top-k run from a shared-memory logit table: one thread per token
 // for up to 32 experts, one warp per token above that.  The gate of choice r
 // is its softmax probability, or -- when renormalising -- exp(g_r - m) over
-// the sum of the k chosen exp(g - m), added in rank order.
+// the sum of the k chosen exp(g - m), added in rank order.  For overflow
+// rerouting the same selection continues for k more ranks: the token's next
+// k experts (its fallbacks) and their softmax probabilities.
 //
 // Inside the layer forward the router also starts the slot assignment: a CTA
 // holds exactly one assignment block of kAssignBlock tokens, so it counts its
@@ -118,7 +120,8 @@ __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
              const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
              float* __restrict__ topk_gate, float* __restrict__ probs, float* __restrict__ logits,
-             const int renorm, const AssignScan scan) {
+             int32_t* __restrict__ fb_idx, float* __restrict__ fb_gate, const int renorm,
+             const AssignScan scan) {
     constexpr int S = route_stages<T>();
     constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
     constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
@@ -221,6 +224,7 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
         for (int i = tid; i < k * E; i += kRouteThreads) cnt[i] = 0;
     __syncthreads();
     const bool count = scan.hist != nullptr;
+    const int kr = fb_idx ? 2 * k : k;  // ranks selected: the choices, then the fallbacks
 
     if (E <= 32) {
         // softmax + top-k: one thread per token
@@ -236,7 +240,7 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                 for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = expf(gl[e] - m) * inv;
             uint32_t taken = 0;
             float chosen[8];
-            for (int r = 0; r < k; ++r) {
+            for (int r = 0; r < kr; ++r) {
                 int be = -1;
                 float bv = -CUDART_INF_F;
                 for (int e = 0; e < E; ++e) {
@@ -247,6 +251,11 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                     }
                 }
                 taken |= 1u << be;
+                if (r >= k) {
+                    fb_idx[(size_t)t * k + r - k] = be;
+                    if (fb_gate) fb_gate[(size_t)t * k + r - k] = expf(bv - m) * inv;
+                    continue;
+                }
                 chosen[r] = bv;
                 if (topk_idx) topk_idx[(size_t)t * k + r] = be;
                 if (count) atomicAdd(&cnt[r * E + be], 1);
@@ -285,7 +294,7 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
             }
             uint32_t taken = 0;
             float chosen[8];
-            for (int r = 0; r < k; ++r) {
+            for (int r = 0; r < kr; ++r) {
                 float bv = -CUDART_INF_F;
                 int be = 0x7fffffff;
 #pragma unroll
@@ -307,6 +316,13 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                     }
                 }
                 if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                if (r >= k) {
+                    if (lane == 0) {
+                        fb_idx[(size_t)t * k + r - k] = be;
+                        if (fb_gate) fb_gate[(size_t)t * k + r - k] = expf(bv - m) * inv;
+                    }
+                    continue;
+                }
                 chosen[r] = bv;
                 if (lane == 0) {
                     if (topk_idx) topk_idx[(size_t)t * k + r] = be;
@@ -330,15 +346,15 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
 template <typename T, int RE>
 cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, const float* bias,
                             int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
-                            const AssignScan& scan, cudaStream_t s) {
+                            int32_t* fb_idx, float* fb_gate, const AssignScan& scan, cudaStream_t s) {
     const size_t smem = route_smem_bytes<RE>((int)sizeof(T), route_stages<T>(), p.E, p.k);
     auto kern = route_kernel<T, RE>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
     return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, p.T, p.d, p.E, p.k, (const T*)x,
-                    (const T*)Wg, bias, topk_idx, topk_gate, probs, logits, (int)(p.flags & MOE_FLAG_RENORM),
-                    scan);
+                    (const T*)Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx, fb_gate,
+                    (int)(p.flags & MOE_FLAG_RENORM), scan);
 }
 
 // 16 experts per pass for 9..64 experts (measured faster at 64), 8 otherwise
@@ -346,30 +362,36 @@ cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, con
 template <typename T>
 cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
                            int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
-                           const AssignScan& scan, cudaStream_t s) {
+                           int32_t* fb_idx, float* fb_gate, const AssignScan& scan, cudaStream_t s) {
     if (p.E > 8 && p.E <= 64)
-        return launch_route_re<T, 16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, scan, s);
-    return launch_route_re<T, 8>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, scan, s);
+        return launch_route_re<T, 16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx, fb_gate,
+                                      scan, s);
+    return launch_route_re<T, 8>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx, fb_gate, scan, s);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
-                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s, float* logits) {
+                         int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s, float* logits,
+                         int32_t* fallback_idx, float* fallback_gate) {
     if (p.T == 0) return cudaSuccess;
     AssignScan none{};
     if (p.dtype == MOE_BF16)
-        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, none, s);
-    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, none, s);
+        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fallback_idx,
+                                             fallback_gate, none, s);
+    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fallback_idx, fallback_gate,
+                                 none, s);
 }
 
 cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
                                int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
-                               cudaStream_t s) {
+                               cudaStream_t s, int32_t* fallback_idx, float* fallback_gate) {
     if (p.T == 0) return cudaErrorInvalidValue;  // callers handle T = 0 without a launch
     if (p.dtype == MOE_BF16)
-        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, scan, s);
-    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, scan, s);
+        return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, fallback_idx,
+                                             fallback_gate, scan, s);
+    return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, fallback_idx,
+                                 fallback_gate, scan, s);
 }
 
 }  // namespace moe

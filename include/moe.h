@@ -78,11 +78,23 @@ typedef struct {
  * chosen logits) instead of using the plain softmax probabilities. */
 #define MOE_FLAG_RENORM 1
 /* flags: expert-choice routing -- each expert takes its min(C, T) tokens of
- * highest router probability (ties: lower token first) instead of each token
+ * highest router logit (ties: lower token first) instead of each token
  * taking its top-k experts; k is read as the average number of experts per
  * token in the capacity rule.  Not combinable with MOE_FLAG_RENORM; needs
  * T <= 49152. */
 #define MOE_FLAG_EXPERT_CHOICE 2
+/* flags: overflow rerouting -- a choice over its expert's capacity goes to
+ * the token's next-best expert instead of being dropped (notes page,
+ * "Capacity Factor and Token Dropping": tokens routed to a full expert are
+ * dropped or redirected to a secondary expert).  One level: the j-th
+ * overflowing choice of a token (ascending rank) goes to its rank k+j expert,
+ * rerouted assignments take only the capacity the k choices left, in the
+ * same (rank, token) priority, and one that finds its fallback full is
+ * dropped.  Needs 2k <= E; not combinable with MOE_FLAG_RENORM or
+ * MOE_FLAG_EXPERT_CHOICE.  moe_layer_forward(_shared) reroutes by itself;
+ * the step-by-step calls are moe_route_fallback and moe_assign_slots_reroute
+ * (moe_assign_slots rejects the flag). */
+#define MOE_FLAG_REROUTE 4
 
 enum {
     MOE_OK = 0,
@@ -126,6 +138,9 @@ typedef struct {
     size_t logits;         /* float[T * E]: router logits (expert-choice
                               layer forward only)                           */
     size_t sel_row;        /* int32[T * E]: expert-choice row of (t, e) or -1 */
+    size_t fallback_idx;   /* int32[T*k]: next-best experts (rerouting only) */
+    size_t fallback_gate;  /* float[T*k]: their probabilities (rerouting only) */
+    size_t rerouted;       /* int32[1]: rerouted assignments that got a slot */
     size_t total;          /* = moe_workspace_size                           */
 } moe_workspace_layout;
 
@@ -219,7 +234,9 @@ int moe_combine(const moe_problem* p, const void* yd, const int32_t* topk_idx,
 /* The whole layer forward: route, assign, dispatch, expert FFN, combine, on
  * one stream, with no host synchronisation.  bias, W3 (GELU) and residual
  * may be NULL.  Intermediates stay in the workspace regions named by
- * moe_workspace_layout_of (probs are not produced). */
+ * moe_workspace_layout_of (probs are not produced).  With MOE_FLAG_REROUTE
+ * the topk_idx / topk_gate regions end up holding route_idx / route_gate of
+ * moe_assign_slots_reroute. */
 int moe_layer_forward(const moe_problem* p, const void* x, const void* Wg, const float* bias,
                       const void* W1, const void* W3, const void* W2, const void* residual,
                       void* y, void* ws, size_t ws_bytes, void* stream);
@@ -251,6 +268,43 @@ int moe_layer_forward_shared(const moe_problem* p, const void* x, const void* Wg
                              const void* W1, const void* W3, const void* W2, const void* Ws1,
                              const void* Ws3, const void* Ws2, const void* residual, void* y,
                              void* ws, size_t ws_bytes, void* stream);
+
+/* Router for overflow rerouting (p->flags must include MOE_FLAG_REROUTE):
+ * moe_route's outputs plus, per token, the next k experts in the same order
+ * (descending logit, lower index first on ties) after its k choices:
+ *   fallback_idx[t, j]  = the token's rank k+j expert        [T, k] int32
+ *   fallback_gate[t, j] = probs[t, fallback_idx[t, j]]      [T, k] fp32
+ * probs may be NULL.  No workspace. */
+int moe_route_fallback(const moe_problem* p, const void* x, const void* Wg, const float* bias,
+                       int32_t* topk_idx, float* topk_gate, int32_t* fallback_idx,
+                       float* fallback_gate, float* probs, void* stream);
+
+/* Slot assignment with overflow rerouting (p->flags must include
+ * MOE_FLAG_REROUTE).  First pass: the assignment of moe_assign_slots on the
+ * k choices.  Second pass: the j-th overflowing choice of token t (ascending
+ * rank) moves to fallback j; in (rank, token) priority the moved assignments
+ * take positions from the expert's first-pass kept count on, kept iff
+ * below C_expert.
+ *   route_idx[t, r]   = the expert serving (t, r): its choice, or the
+ *                       fallback it moved to                  [T, k] int32
+ *   route_gate[t, r]  = that expert's gate (topk_gate, or fallback_gate)
+ *   slot_pos[t, r]    = its position at route_idx, or -1 when it has none
+ *   counts_routed     = first-pass assignments per expert (as moe_assign_slots)
+ *   counts_kept       = rows per expert after rerouting (<= C_expert)
+ *   expert_offsets, shard_offsets, row_token: of the rows after rerouting
+ *   shard_routed, shard_overflow: of the k choices (as moe_assign_slots)
+ *   dropped[0]  = assignments with no slot at the end      (may be NULL)
+ *   rerouted[0] = moved assignments that got a slot         (may be NULL)
+ * route_idx / route_gate may be the same buffers as topk_idx / topk_gate
+ * (updated in place).  moe_combine takes route_idx, slot_pos, route_gate.
+ * Uses the workspace's hist region and status word. */
+int moe_assign_slots_reroute(const moe_problem* p, const int32_t* topk_idx, const float* topk_gate,
+                             const int32_t* fallback_idx, const float* fallback_gate,
+                             int32_t* route_idx, float* route_gate, int32_t* slot_pos,
+                             int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
+                             int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
+                             int32_t* row_token, int32_t* dropped, int32_t* rerouted, void* ws,
+                             size_t ws_bytes, void* stream);
 
 /* Router logits and probabilities without the top-k: logits [T, E] fp32 in
  * the router's fixed order (bias included, as moe_route computes them),

@@ -59,6 +59,7 @@ class Workload:
     renorm: bool = False            # renormalise the k gates of a token to sum to one
     ffn_shared: int = 0             # width of a shared expert every token goes through; 0 = none
     expert_choice: bool = False     # experts take their tokens (instead of tokens their experts)
+    reroute: bool = False           # a choice over capacity moves to the token's next-best expert
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)

@@ -33,7 +33,7 @@ def _declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
-    assert len(names) == 19, names
+    assert len(names) == 21, names
     assert sorted(moe.EXPORTS) == names
     lib = moe.load()
     for n in names:
@@ -67,6 +67,9 @@ def _problem(**kw):
     (dict(T=1 << 30, k=2), moe.MOE_ERR_UNSUPPORTED),
     (dict(dtype=7), moe.MOE_ERR_INVALID_ARG),
     (dict(act=5), moe.MOE_ERR_INVALID_ARG),
+    (dict(reroute=True, E=8, D=4, k=5), moe.MOE_ERR_INVALID_ARG),    # needs 2k <= E
+    (dict(reroute=True, renorm=True), moe.MOE_ERR_INVALID_ARG),
+    (dict(reroute=True, expert_choice=True), moe.MOE_ERR_INVALID_ARG),
 ])
 def test_invalid_problems_rejected(kw, code):
     p = _problem(**kw)
@@ -103,6 +106,12 @@ def test_workspace_layout_is_aligned_and_disjoint():
                      ffn_sync=4 * (1 + wl.E * -(-(-(-C // 128)) // 2)),
                      stats=8 * min(64, max(1, -(-wl.T // 64))) * (wl.E + 1))
         spans = sorted((L[n], L[n] + s) for n, s in sizes.items())
+        # rerouting adds the fallback choices (and the rerouted count) to the same layout
+        Lr = moe.moe_workspace_layout_of(moe.problem_of(wl.with_(reroute=True))) if 2 * wl.k <= wl.E else None
+        if Lr is not None:
+            assert all(Lr[n] == L[n] for n in sizes)
+            assert Lr["fallback_gate"] - Lr["fallback_idx"] >= 4 * Tk
+            assert Lr["rerouted"] - Lr["fallback_gate"] >= 4 * Tk and Lr["total"] >= Lr["rerouted"] + 4
         assert spans[0][0] == 0 == L["status"]
         for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
             assert a1 <= b0
@@ -135,6 +144,27 @@ def test_bad_pointers_and_workspace_rejected_before_launch():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_combine(p, A, A, A, A, A, A + 2, A, stream=0)
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG  # misaligned residual
+    # rerouting: the plain slot calls refuse the flag, the rerouting calls need it
+    pr = _problem(reroute=True)
+    need_r = moe.moe_workspace_size(pr)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_assign_slots(pr, A, A, A, A, A, A, A, A, A, None, A, need_r, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_assign_slots_static(pr, A, A, A, A, A, A, A, A, A, None, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_assign_slots_reroute(p, *([A] * 14), None, None, A, need, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_route_fallback(p, A, A, None, A, A, A, A, None, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_route_fallback(pr, A, A, None, A, A, None, A, None, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG  # fallback_idx missing
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_assign_slots_reroute(pr, *([A] * 14), None, None, A, need_r - 1, stream=0)
+    assert ei.value.status == moe.MOE_ERR_WORKSPACE
 
 
 def test_empty_batch_is_a_no_op():
