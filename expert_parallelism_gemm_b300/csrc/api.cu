@@ -114,7 +114,7 @@ void layout(const Problem& p, moe_workspace_layout* L) {
     L->h = take(rm * p.ffn * eb);
     L->yd = take(rm * p.d * eb);
     L->ffn_sync = take(ffn_sync_ints(p) * sizeof(int32_t));
-    L->stats = take((size_t)stats_blocks(p.T) * (size_t)(p.E + 1) * sizeof(double));
+    L->stats = take((size_t)(p.E + 1) * sizeof(unsigned long long));
     const size_t Ts = p.ffn_shared > 0 ? (size_t)p.T : 0;
     L->hs = take(Ts * p.ffn_shared * eb);
     L->ys = take(Ts * p.d * eb);
@@ -486,13 +486,14 @@ int moe_routing_stats(const moe_problem* mp, const float* probs, const int32_t* 
     int rc = to_problem(mp, &p);
     if (rc != MOE_OK) return rc;
     if ((p.T > 0 && !probs) || !counts_routed || !counts_kept || !stats) return MOE_ERR_INVALID_ARG;
+    if (p.T > ((int64_t)1 << 25)) return MOE_ERR_UNSUPPORTED;  // the 64-bit fixed-point sums
     moe_workspace_layout L;
     rc = check_ws(p, ws, ws_bytes, &L);
     if (rc != MOE_OK) return rc;
     char* w = (char*)ws;
     // status[2] is the statistics kernel's completion ticket
     return cuda_rc(launch_routing_stats(p, probs, counts_routed, counts_kept, stats, mean_prob,
-                                        (double*)(w + L.stats), (unsigned*)(w + L.status) + 2,
+                                        (unsigned long long*)(w + L.stats), (unsigned*)(w + L.status) + 2,
                                         (cudaStream_t)stream));
 }
 

@@ -180,12 +180,12 @@ cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk
                            const float* topk_gate, const void* residual, void* y, cudaStream_t s,
                            const void* shared = nullptr);
 
-// routing statistics: `partials` holds stats_blocks(T) x (E+1) doubles,
-// `ticket` is zero before the launch and left zero
+// routing statistics: `acc` holds E+1 64-bit fixed-point sums and `ticket`
+// one int, both zero before the launch and left zero
 int64_t stats_blocks(int64_t T);
 cudaError_t launch_routing_stats(const Problem& p, const float* probs, const int32_t* counts_routed,
                                  const int32_t* counts_kept, float* stats, float* mean_prob,
-                                 double* partials, unsigned* ticket, cudaStream_t s);
+                                 unsigned long long* acc, unsigned* ticket, cudaStream_t s);
 
 // expert-choice routing (ec.cu)
 cudaError_t launch_ec_select(const Problem& p, const float* logits, int32_t* row_token, int32_t* expert_offsets,

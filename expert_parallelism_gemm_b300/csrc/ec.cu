@@ -17,7 +17,7 @@
 // non-negative values, all bits flipped for negative ones, -0 read as +0) and
 // finds the Cc-th largest key K by an 8-bit radix select
 // (four histogram passes, most significant digit first, integer shared-memory
-// counts).  A token is taken if its key is above K, or equal to K and among
+// counts; one warp scans the 256 bins to find each digit).  A token is taken if its key is above K, or equal to K and among
 // the first (Cc - number above K) equal keys in token order; rows follow from
 // a block-wide scan of the taken flags in token order.  Integer work only, so
 // the selection is exact and does not depend on scheduling.
@@ -100,15 +100,31 @@ ec_select_kernel(int64_t T, int E, int64_t Cc, const float* __restrict__ logits,
                 if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1);
             }
             __syncthreads();
-            if (tid == 0) {
-                int want = s_want, cum = 0;
-                for (int b = 255; b >= 0; --b) {
-                    if (cum + hist[b] >= want) {
-                        s_prefix = prefix | ((uint32_t)b << shift);
+            if (tid < 32) {
+                // the digit holding the want-th largest key: lane l takes the
+                // bins 255 - 8l .. 248 - 8l (descending), a warp scan gives the
+                // count of keys in the bins above them, and the one bin where
+                // the running count first reaches want is the digit
+                const int want = s_want;
+                int loc = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) loc += hist[255 - 8 * tid - j];
+                __syncwarp();  // every lane has read s_want before one lane rewrites it
+                int incl = loc;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += n;
+                }
+                int cum = incl - loc;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int h = hist[255 - 8 * tid - j];
+                    if (cum < want && cum + h >= want) {
+                        s_prefix = prefix | ((uint32_t)(255 - 8 * tid - j) << shift);
                         s_want = want - cum;  // keys equal to the digit prefix still to take
-                        break;
                     }
-                    cum += hist[b];
+                    cum += h;
                 }
             }
             mask |= 255u << shift;

@@ -102,9 +102,17 @@ __device__ __forceinline__ void write_gates(float* gate, const float (&chosen)[8
     for (int r = 0; r < k; ++r) gate[r] = expf(chosen[r] - m) / den;
 }
 
+// ring stages: 4 for bf16 (3 for fp32, whose chunks are twice the bytes);
+// 5 for bf16 at up to 8 experts, where the logit table is small enough that
+// the fifth stage still leaves two CTAs per SM and puts a 1024-wide hidden
+// dimension's four chunks in flight at once
 template <typename T>
 __host__ __device__ constexpr int route_stages() {
     return sizeof(T) == 2 ? 4 : 3;
+}
+template <typename T>
+constexpr int route_stages_small_e() {
+    return sizeof(T) == 2 ? 5 : 3;
 }
 
 // experts per pass: 8, or 16 above 8 experts
@@ -115,14 +123,13 @@ size_t route_smem_bytes(int elem_bytes, int stages, int E, int k) {
            (size_t)k * E * sizeof(int);
 }
 
-template <typename T, int RE>
+template <typename T, int RE, int S>
 __global__ void __launch_bounds__(kRouteThreads)
 route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
              const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
              float* __restrict__ topk_gate, float* __restrict__ probs, float* __restrict__ logits,
              int32_t* __restrict__ fb_idx, float* __restrict__ fb_gate, const int renorm,
              const AssignScan scan) {
-    constexpr int S = route_stages<T>();
     constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
     constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
     constexpr int VPR = RP / 16;                     // 16-byte vectors per ring row
@@ -343,12 +350,12 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     }
 }
 
-template <typename T, int RE>
+template <typename T, int RE, int S>
 cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, const float* bias,
                             int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
                             int32_t* fb_idx, float* fb_gate, const AssignScan& scan, cudaStream_t s) {
-    const size_t smem = route_smem_bytes<RE>((int)sizeof(T), route_stages<T>(), p.E, p.k);
-    auto kern = route_kernel<T, RE>;
+    const size_t smem = route_smem_bytes<RE>((int)sizeof(T), S, p.E, p.k);
+    auto kern = route_kernel<T, RE, S>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
@@ -358,15 +365,19 @@ cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, con
 }
 
 // 16 experts per pass for 9..64 experts (measured faster at 64), 8 otherwise
-// (measured faster at 8 and 128)
+// (measured faster at 8 and 128); the deeper ring for up to 8 experts
 template <typename T>
 cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
                            int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
                            int32_t* fb_idx, float* fb_gate, const AssignScan& scan, cudaStream_t s) {
-    if (p.E > 8 && p.E <= 64)
-        return launch_route_re<T, 16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx, fb_gate,
-                                      scan, s);
-    return launch_route_re<T, 8>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx, fb_gate, scan, s);
+    if (p.E <= 8)
+        return launch_route_re<T, 8, route_stages_small_e<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits,
+                                                                fb_idx, fb_gate, scan, s);
+    if (p.E <= 64)
+        return launch_route_re<T, 16, route_stages<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits,
+                                                         fb_idx, fb_gate, scan, s);
+    return launch_route_re<T, 8, route_stages<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx,
+                                                    fb_gate, scan, s);
 }
 
 }  // namespace

@@ -129,7 +129,7 @@ typedef struct {
     size_t ffn_sync;       /* int32 scratch of the expert FFN (gate/up ->
                               down release counters); every call leaves it
                               zero again                                    */
-    size_t stats;          /* double scratch of moe_routing_stats            */
+    size_t stats;          /* uint64[E+1] sums of moe_routing_stats (left zero) */
     size_t hs;             /* dtype[T * ffn_shared]: shared-expert hidden rows */
     size_t ys;             /* dtype[T * d]: shared-expert outputs            */
     size_t shared_sync;    /* int32 scratch of the shared-expert FFN         */
@@ -380,9 +380,11 @@ enum {
  *   stats[MOE_STAT_IMBALANCE] = max_e counts_routed[e] / (T*k/E)
  *   mean_prob[e]              = P_e                   (may be NULL)
  * probs: [T, E] fp32, counts: [E] int32, stats: float[MOE_NUM_STATS], all
- * device pointers.  Deterministic (fixed-order fp64 sums).  Uses the
- * workspace's stats region and a ticket in its status region; T = 0 gives
- * zeros. */
+ * device pointers.  Deterministic: the sums over tokens are 64-bit
+ * fixed-point integers (units of 2^-36), the final combination one fixed-order
+ * fp32 pass.  Needs T <= 2^25 (else MOE_ERR_UNSUPPORTED).  Uses the
+ * workspace's stats region (left zero) and a ticket in its status region;
+ * T = 0 gives zeros. */
 int moe_routing_stats(const moe_problem* p, const float* probs, const int32_t* counts_routed,
                       const int32_t* counts_kept, float* stats, float* mean_prob,
                       void* ws, size_t ws_bytes, void* stream);

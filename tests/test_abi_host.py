@@ -104,7 +104,7 @@ def test_workspace_layout_is_aligned_and_disjoint():
                      dropped=4, hist=4 * wl.E * wl.k * nblk, row_token=4 * rows_max,
                      xd=eb * rows_max * wl.d, h=eb * rows_max * wl.ffn, yd=eb * rows_max * wl.d,
                      ffn_sync=4 * (1 + wl.E * -(-(-(-C // 128)) // 2)),
-                     stats=8 * min(64, max(1, -(-wl.T // 64))) * (wl.E + 1))
+                     stats=8 * (wl.E + 1))
         spans = sorted((L[n], L[n] + s) for n, s in sizes.items())
         # rerouting adds the fallback choices (and the rerouted count) to the same layout
         Lr = moe.moe_workspace_layout_of(moe.problem_of(wl.with_(reroute=True))) if 2 * wl.k <= wl.E else None
