@@ -27,6 +27,7 @@ on the same workload, each step a bounded sample, on rank 0 only.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -347,79 +348,60 @@ def run_ours(args, rank, world, local_rank):
         rr_stats["kept"] = int(moe.workspace_view(rws, rp, "expert_offsets", torch.int32, wl.E + 1)[-1].item())
         del rws
 
-    # ---- end to end through moe_layer_forward with host buffers
-    x_host = inp.x.cpu().pin_memory()
-    y_host = torch.empty(wl.T, wl.d, dtype=inp.x.dtype).pin_memory()
-    x_dev = torch.empty_like(inp.x)
+    # ---- end to end through moe_layer_forward_host: every step copies its x
+    # in from page-locked host memory (moe_host_alloc) and its y back out.
+    # Serial: one step per call, L2 flushed before each.  Pipelined (the e2e
+    # value): K steps in one call, step i's input copy overlapping step i-1's
+    # layer and step i-2's output copy on the library's copy streams; no L2
+    # flush there, as x arrives from the host every step and the 176 MB of
+    # expert weights the layer streams exceed L2.
+    eb_ = inp.x.element_size()
+    nbytes = wl.T * wl.d * eb_
+    hx = [moe.moe_host_alloc(nbytes) for _ in range(2)]
+    hy = [moe.moe_host_alloc(nbytes) for _ in range(2)]
+    # written by one thread: host lines left dirty in many cores' caches by a
+    # multi-threaded fill made every later copy from them ~5x slower here
+    x_bytes = inp.x.cpu().contiguous().view(torch.uint8).numpy().reshape(-1)
+    for a in hx:
+        np.copyto(np.ctypeslib.as_array((ctypes.c_uint8 * nbytes).from_address(a)), x_bytes)
+    stg_bytes = moe.moe_host_staging_size(p)
+    staging = torch.empty(stg_bytes, dtype=torch.uint8, device=dev)
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        moe.moe_layer_forward(p, x_dev, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y, ws, wsb,
-                              stream)
-        y_host.copy_(y, non_blocking=True)
+    def host_run(n):
+        moe.moe_layer_forward_host(p, [hx[i % 2] for i in range(n)], inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2,
+                                   [hy[i % 2] for i in range(n)], staging, stg_bytes, ws, wsb, stream)
 
     for _ in range(max(1, args.warmup)):
         flush()
-        e2e_step()
+        host_run(1)
     e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
         flush()
         e_s[i].record(stream)
-        e2e_step()
+        host_run(1)
         e_e[i].record(stream)
     barrier()
     e2e_serial_ms_max = max_over_ranks(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)), world, dev)
 
-    # ---- end to end as a serving loop runs it: step i's input copy overlaps
-    # step i-1's layer and step i-2's output copy (three streams, two device
-    # buffers each for x and y, events order the reuse); every step still
-    # copies its x in from pinned host memory and its y back out, and the
-    # timed region runs from the first input copy to the last output copy.
-    # No L2 flush: x arrives from the host each step and the 176 MB of expert
-    # weights the layer streams exceed L2.
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    x_buf = [torch.empty_like(inp.x) for _ in range(2)]
-    y_buf = [torch.empty_like(y) for _ in range(2)]
-    y_hosts = [torch.empty(wl.T, wl.d, dtype=inp.x.dtype).pin_memory() for _ in range(2)]
-
-    def pipelined(n_steps):
-        ev = lambda: torch.cuda.Event(enable_timing=False)
-        in_done, comp_done, out_done = [], [], []
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(s_in)
-        for i in range(n_steps):
-            b = i % 2
-            if i >= 2:
-                s_in.wait_event(comp_done[i - 2])  # x_buf[b] no longer read
-            with torch.cuda.stream(s_in):
-                x_buf[b].copy_(x_host, non_blocking=True)
-            in_done.append(ev())
-            in_done[i].record(s_in)
-            stream.wait_event(in_done[i])
-            if i >= 2:
-                stream.wait_event(out_done[i - 2])  # y_buf[b] copied out
-            moe.moe_layer_forward(p, x_buf[b], inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2, None, y_buf[b], ws, wsb,
-                                  stream)
-            comp_done.append(ev())
-            comp_done[i].record(stream)
-            s_out.wait_event(comp_done[i])
-            with torch.cuda.stream(s_out):
-                y_hosts[b].copy_(y_buf[b], non_blocking=True)
-            out_done.append(ev())
-            out_done[i].record(s_out)
-        t_end.record(s_out)
-        return t_start, t_end
-
-    pipelined(max(3, args.warmup))
+    host_run(max(3, args.warmup))
     barrier()
-    t_start, t_end = pipelined(args.steps)
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    host_run(args.steps)
+    t_end.record(stream)
     barrier()
     e2e_ms_max = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
-    if not torch.equal(y_hosts[(args.steps - 1) % 2], y.cpu()):
-        raise RuntimeError("pipelined end-to-end output differs from the device step's output")
+    y_last = moe.host_tensor(hy[(args.steps - 1) % 2], (wl.T, wl.d), inp.x.dtype).clone()
+    for a in hx + hy:
+        moe.moe_host_free(a)
+    if moe.moe_device_status(ws, stream) != moe.MOE_OK:
+        raise RuntimeError("device status after the end-to-end loops")
+    step()
+    torch.cuda.synchronize(dev)
+    if not torch.equal(y_last, y.cpu()):
+        raise RuntimeError("end-to-end output differs from the device step's output")
 
     out = None
     if rank == 0:
@@ -489,11 +471,11 @@ def run_ours(args, rank, world, local_rank):
             "e2e": {"value": job_tokens_per_s(wl.T, world, args.steps, e2e_ms_max), "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * eb,
                     "ms_per_step": e2e_ms_max / args.steps,
-                    "api": "moe_layer_forward, pinned host x -> device -> host y every step; copies of "
-                           "neighbouring steps overlap the layer on separate streams",
+                    "api": "moe_layer_forward_host: K steps, x copied in from page-locked host memory and y "
+                           "copied out every step, copies of neighbouring steps overlapping the layer",
                     "serial": {"value": job_tokens_per_s(wl.T, world, args.steps, e2e_serial_ms_max),
                                "ms_per_step": e2e_serial_ms_max / args.steps,
-                               "note": "each step's copy in, layer and copy out back to back, L2 flushed"}},
+                               "note": "one step per moe_layer_forward_host call, L2 flushed before each"}},
             "gpu_launches": args.steps * launches_per_step(wl),
             "clocks": clocks,
         }

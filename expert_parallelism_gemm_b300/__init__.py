@@ -33,7 +33,8 @@ EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe
            "moe_assign_slots_static", "moe_routing_stats", "moe_shared_expert_ffn",
            "moe_combine_shared", "moe_layer_forward_shared", "moe_expert_choice_assign",
            "moe_combine_expert_choice", "moe_router_logits", "moe_route_fallback",
-           "moe_assign_slots_reroute")
+           "moe_assign_slots_reroute", "moe_host_alloc", "moe_host_free", "moe_host_staging_size",
+           "moe_layer_forward_host")
 
 
 class moe_problem(ctypes.Structure):
@@ -94,6 +95,10 @@ def load() -> ctypes.CDLL:
     lib.moe_combine_expert_choice.argtypes = [PP, P, P, P, P, P, P, P]
     lib.moe_route_fallback.argtypes = [PP] + [P] * 9
     lib.moe_assign_slots_reroute.argtypes = [PP] + [P] * 17 + [sz, P]
+    lib.moe_host_alloc.argtypes = [sz, ctypes.POINTER(ctypes.c_void_p)]
+    lib.moe_host_free.argtypes = [P]
+    lib.moe_host_staging_size.argtypes = [PP, ctypes.POINTER(ctypes.c_size_t)]
+    lib.moe_layer_forward_host.argtypes = [PP, ctypes.c_int64, P, P, P, P, P, P, P, P, sz, P, sz, P]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for n in EXPORTS:
@@ -288,6 +293,49 @@ def moe_routing_stats(problem, probs, counts_routed, counts_kept, stats, mean_pr
     _check(load().moe_routing_stats(ctypes.byref(problem), _p(probs), _p(counts_routed),
                                     _p(counts_kept), _p(stats), _p(mean_prob), _p(ws), int(ws_bytes),
                                     _stream(stream)), "moe_routing_stats")
+
+
+def moe_host_alloc(nbytes: int) -> int:
+    """Page-locked host memory (address as an int; 0 for nbytes == 0)."""
+    ptr = ctypes.c_void_p()
+    _check(load().moe_host_alloc(int(nbytes), ctypes.byref(ptr)), "moe_host_alloc")
+    return ptr.value or 0
+
+
+def moe_host_free(ptr: int):
+    _check(load().moe_host_free(ptr or None), "moe_host_free")
+
+
+def host_tensor(ptr: int, shape, dtype):
+    """CPU tensor viewing host memory at `ptr` (e.g. from moe_host_alloc)."""
+    import torch
+    n = 1
+    for v in shape:
+        n *= int(v)
+    item = torch.empty((), dtype=dtype).element_size()
+    buf = (ctypes.c_char * (n * item)).from_address(ptr)
+    return torch.frombuffer(buf, dtype=torch.uint8).view(dtype).view(*shape)
+
+
+def moe_host_staging_size(problem: moe_problem) -> int:
+    n = ctypes.c_size_t()
+    _check(load().moe_host_staging_size(ctypes.byref(problem), ctypes.byref(n)), "moe_host_staging_size")
+    return n.value
+
+
+def moe_layer_forward_host(problem, x_hosts, Wg, bias, W1, W3, W2, y_hosts, staging, staging_bytes, ws,
+                           ws_bytes, stream=None):
+    """len(x_hosts) steps of the layer from host buffers (addresses or CPU
+    tensors), copies overlapped with the layers; see include/moe.h."""
+    n = len(x_hosts)
+    if len(y_hosts) != n:
+        raise ValueError("x_hosts and y_hosts differ in length")
+    xs = (ctypes.c_void_p * max(n, 1))(*[_p(t) for t in x_hosts])
+    ys = (ctypes.c_void_p * max(n, 1))(*[_p(t) for t in y_hosts])
+    _check(load().moe_layer_forward_host(ctypes.byref(problem), n, xs, _p(Wg), _p(bias), _p(W1), _p(W3),
+                                         _p(W2), ys, _p(staging), int(staging_bytes), _p(ws), int(ws_bytes),
+                                         _stream(stream)),
+           "moe_layer_forward_host")
 
 
 def moe_device_status(ws, stream=None) -> int:

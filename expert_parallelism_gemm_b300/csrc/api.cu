@@ -4,6 +4,7 @@
 // moe_device_status, whose job it is).
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 
 #include "assign_scan.cuh"
 
@@ -234,6 +235,39 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
                : launch_combine(p, yd, idx, slot, off, gate, residual, y, s, ys);
     return cuda_rc(e);
 }
+
+// ---- host pipeline: the copy streams and events of moe_layer_forward_host,
+// made once per device and kept for the life of the process
+struct HostPipe {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr, in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+    bool ready = false;
+};
+constexpr int kMaxDevices = 64;
+HostPipe g_pipes[kMaxDevices];
+std::mutex g_pipe_mu;
+
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe& hp = g_pipes[dev];
+    if (!hp.ready) {
+        bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; ok && i < 2; ++i)
+            ok = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.comp_done[i], cudaEventDisableTiming) == cudaSuccess &&
+                 cudaEventCreateWithFlags(&hp.out_done[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) return MOE_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return MOE_OK;
+}
+
+size_t host_staging_bytes(const Problem& p) { return 4 * align256((size_t)p.T * p.d * esize(p.dtype)); }
 
 }  // namespace
 }  // namespace moe
@@ -495,6 +529,79 @@ int moe_routing_stats(const moe_problem* mp, const float* probs, const int32_t* 
     return cuda_rc(launch_routing_stats(p, probs, counts_routed, counts_kept, stats, mean_prob,
                                         (unsigned long long*)(w + L.stats), (unsigned*)(w + L.status) + 2,
                                         (cudaStream_t)stream));
+}
+
+int moe_host_alloc(size_t bytes, void** ptr) {
+    if (!ptr) return MOE_ERR_INVALID_ARG;
+    *ptr = nullptr;
+    if (bytes == 0) return MOE_OK;
+    return cudaHostAlloc(ptr, bytes, cudaHostAllocPortable) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_host_free(void* ptr) {
+    if (!ptr) return MOE_OK;
+    return cudaFreeHost(ptr) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_host_staging_size(const moe_problem* mp, size_t* bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    *bytes = host_staging_bytes(p);
+    return MOE_OK;
+}
+
+int moe_layer_forward_host(const moe_problem* mp, int64_t n_steps, const void* const* x_host, const void* Wg,
+                           const float* bias, const void* W1, const void* W3, const void* W2,
+                           void* const* y_host, void* staging, size_t staging_bytes, void* ws, size_t ws_bytes,
+                           void* stream) {
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.ffn_shared != 0 || n_steps < 0) return MOE_ERR_INVALID_ARG;
+    if (n_steps == 0 || p.T == 0) return MOE_OK;
+    if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < n_steps; ++i)
+        if (!x_host[i] || !y_host[i]) return MOE_ERR_INVALID_ARG;
+    const size_t xb = (size_t)p.T * p.d * esize(p.dtype), slot = align256(xb);
+    if (!staging || staging_bytes < host_staging_bytes(p) || !aligned16(staging)) return MOE_ERR_WORKSPACE;
+    moe_workspace_layout L;
+    rc = check_ws(p, ws, ws_bytes, &L);
+    if (rc != MOE_OK) return rc;
+    HostPipe* hp = nullptr;
+    rc = host_pipe(&hp);
+    if (rc != MOE_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    char* st = (char*)staging;
+    void* xs[2] = {st, st + slot};
+    void* ys[2] = {st + 2 * slot, st + 3 * slot};
+    auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+    // the copies start after the work already queued on `stream`
+    if (!ck(cudaEventRecord(hp->start, s)) || !ck(cudaStreamWaitEvent(hp->in, hp->start, 0)) ||
+        !ck(cudaStreamWaitEvent(hp->out, hp->start, 0)))
+        return MOE_ERR_CUDA;
+    for (int64_t i = 0; i < n_steps; ++i) {
+        const int b = (int)(i & 1);
+        // x buffer b is free once step i-2's layer has read it
+        if (i >= 2 && !ck(cudaStreamWaitEvent(hp->in, hp->comp_done[b], 0))) return MOE_ERR_CUDA;
+        if (!ck(cudaMemcpyAsync(xs[b], x_host[i], xb, cudaMemcpyHostToDevice, hp->in)) ||
+            !ck(cudaEventRecord(hp->in_done[b], hp->in)) || !ck(cudaStreamWaitEvent(s, hp->in_done[b], 0)))
+            return MOE_ERR_CUDA;
+        // y buffer b is free once step i-2's output copy has read it
+        if (i >= 2 && !ck(cudaStreamWaitEvent(s, hp->out_done[b], 0))) return MOE_ERR_CUDA;
+        rc = layer_forward(mp, xs[b], Wg, bias, W1, W3, W2, nullptr, nullptr, nullptr, nullptr, ys[b], ws, ws_bytes,
+                           stream);
+        if (rc != MOE_OK) return rc;
+        if (!ck(cudaEventRecord(hp->comp_done[b], s)) || !ck(cudaStreamWaitEvent(hp->out, hp->comp_done[b], 0)) ||
+            !ck(cudaMemcpyAsync(y_host[i], ys[b], xb, cudaMemcpyDeviceToHost, hp->out)) ||
+            !ck(cudaEventRecord(hp->out_done[b], hp->out)))
+            return MOE_ERR_CUDA;
+    }
+    // `stream` completes only after every output copy
+    for (int b = 0; b < 2 && b < n_steps; ++b)
+        if (!ck(cudaStreamWaitEvent(s, hp->out_done[b], 0))) return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 int moe_device_status(void* ws, void* stream) {

@@ -33,7 +33,7 @@ def _declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
-    assert len(names) == 21, names
+    assert len(names) == 25, names
     assert sorted(moe.EXPORTS) == names
     lib = moe.load()
     for n in names:
@@ -165,6 +165,28 @@ def test_bad_pointers_and_workspace_rejected_before_launch():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_assign_slots_reroute(pr, *([A] * 14), None, None, A, need_r - 1, stream=0)
     assert ei.value.status == moe.MOE_ERR_WORKSPACE
+
+
+def test_host_path_rejects_bad_arguments_before_any_cuda_call():
+    p = _problem()
+    need = moe.moe_workspace_size(p)
+    stg = moe.moe_host_staging_size(p)
+    assert stg == 4 * (-(-(128 * 64 * 2) // 256) * 256)
+    A = 1 << 20
+    for kw, code in [(dict(staging_bytes=stg - 1), moe.MOE_ERR_WORKSPACE),
+                     (dict(ws_bytes=need - 1), moe.MOE_ERR_WORKSPACE),
+                     (dict(x=[None]), moe.MOE_ERR_INVALID_ARG)]:
+        args = dict(x=[A], y=[A], staging_bytes=stg, ws_bytes=need)
+        args.update(kw)
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_layer_forward_host(p, args["x"], A, None, A, A, A, args["y"], A, args["staging_bytes"], A,
+                                       args["ws_bytes"], stream=0)
+        assert ei.value.status == code
+    with pytest.raises(moe.MoeError) as ei:  # a shared expert needs the device entry point
+        moe.moe_layer_forward_host(_problem(ffn_shared=64), [A], A, None, A, A, A, [A], A, stg, A, need, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    # no steps: nothing to do
+    moe.moe_layer_forward_host(p, [], A, None, A, A, A, [], A, stg, A, need, stream=0)
 
 
 def test_empty_batch_is_a_no_op():
