@@ -76,6 +76,25 @@ __device__ __forceinline__ void load8(const uint8_t* p, float (&v)[8], float*) {
     v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
 }
 
+// acc = fma(x[j], w[j], acc) for the 8 bf16 elements j = 0..7 of a 16-byte
+// vector pair, in ascending j (element 2i is the low half of word i).  The
+// mixed-precision FMA takes the bf16 halves as they are: widening bf16 to fp32
+// is exact, so each step rounds exactly as fmaf on the widened values does,
+// and no unpacking instructions are spent.
+__device__ __forceinline__ void fma8_bf16(float& acc, const uint4& x, const uint4& w) {
+    asm("{\n"
+        " .reg .b16 x0, x1, x2, x3, x4, x5, x6, x7, w0, w1, w2, w3, w4, w5, w6, w7;\n"
+        " mov.b32 {x0, x1}, %1;\n mov.b32 {x2, x3}, %2;\n mov.b32 {x4, x5}, %3;\n mov.b32 {x6, x7}, %4;\n"
+        " mov.b32 {w0, w1}, %5;\n mov.b32 {w2, w3}, %6;\n mov.b32 {w4, w5}, %7;\n mov.b32 {w6, w7}, %8;\n"
+        " fma.rn.f32.bf16 %0, x0, w0, %0;\n fma.rn.f32.bf16 %0, x1, w1, %0;\n"
+        " fma.rn.f32.bf16 %0, x2, w2, %0;\n fma.rn.f32.bf16 %0, x3, w3, %0;\n"
+        " fma.rn.f32.bf16 %0, x4, w4, %0;\n fma.rn.f32.bf16 %0, x5, w5, %0;\n"
+        " fma.rn.f32.bf16 %0, x6, w6, %0;\n fma.rn.f32.bf16 %0, x7, w7, %0;\n"
+        "}"
+        : "+f"(acc)
+        : "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));
+}
+
 // One reduce-scatter round of the butterfly over offset O: of the N values
 // a[0..N), keep the half chosen by bit O of the lane and add the partner's.
 template <int O, int N, int M>
@@ -153,26 +172,38 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     dep_release();
 
     // copies of flattened chunk q = (pass, chunk) into ring slot q % S; always
-    // commits a group
+    // commits a group.  Thread tid copies the 16-byte column colv of rows
+    // row0, row0 + RPI, ...: the first kTok / RPI of them x rows (token
+    // pointers fixed for the CTA), the rest the pass's Wg rows.
+    constexpr int RPI = kRouteThreads / VPR;  // rows per sweep of the CTA's threads
+    constexpr int NX = kTok / RPI, NI = kStageRows / RPI;
+    static_assert(kTok % RPI == 0 && kStageRows % RPI == 0, "rows split evenly over the threads");
+    const int row0 = tid / VPR, colv = (tid % VPR) * VE;
+    const T* xrow[NX];
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+        const int64_t t = t0 + row0 + RPI * i;
+        xrow[i] = t < T_ ? x + (size_t)t * d + colv : nullptr;
+    }
     auto issue = [&](int q) {
         if (q < nq) {
             const int pass = q / nchunks, c = q - pass * nchunks;
             const int k0 = c * kKC;
-            const uint32_t slot = ring_s + (uint32_t)((q % S) * kStageRows * RP);
-            for (int v = tid; v < kStageRows * VPR; v += kRouteThreads) {
-                const int row = v / VPR, col = (v % VPR) * VE;
-                const bool in_d = k0 + col < d;  // d is a multiple of VE
-                const T* src;
-                bool ok;
-                if (row < kTok) {
-                    ok = in_d && t0 + row < T_;
-                    src = x + (ok ? (size_t)(t0 + row) * d + k0 + col : 0);
-                } else {
-                    const int e = pass * RE + row - kTok;
-                    ok = in_d && e < E;
-                    src = Wg + (ok ? (size_t)e * d + k0 + col : 0);
-                }
-                cp_async16(slot + (uint32_t)(row * RP + col * (int)sizeof(T)), src, ok ? 16u : 0u);
+            const bool in_d = k0 + colv < d;  // d is a multiple of VE
+            const uint32_t slot =
+                ring_s + (uint32_t)((q % S) * kStageRows * RP + colv * (int)sizeof(T) + row0 * RP);
+#pragma unroll
+            for (int i = 0; i < NX; ++i) {
+                const bool ok = in_d && xrow[i] != nullptr;
+                cp_async16(slot + (uint32_t)(RPI * i * RP), ok ? (const void*)(xrow[i] + k0) : (const void*)x,
+                           ok ? 16u : 0u);
+            }
+#pragma unroll
+            for (int i = NX; i < NI; ++i) {
+                const int e = pass * RE + row0 + RPI * i - kTok;
+                const bool ok = in_d && e < E;
+                cp_async16(slot + (uint32_t)(RPI * i * RP), Wg + (ok ? (size_t)e * d + k0 + colv : 0),
+                           ok ? 16u : 0u);
             }
         }
         cp_async_commit();
@@ -190,17 +221,31 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
         __syncthreads();  // chunk q visible; every thread is done with chunk q-1
         issue(q + S - 1);  // into the slot chunk q-1 used
         const uint8_t* base = ring + (size_t)(q % S) * kStageRows * RP + lane * 8 * (int)sizeof(T);
-        float xv[kRT][8];
+        if constexpr (sizeof(T) == 2) {
+            uint4 xq[kRT];
 #pragma unroll
-        for (int rt = 0; rt < kRT; ++rt) load8(base + (size_t)(kRT * warp + rt) * RP, xv[rt], (T*)nullptr);
+            for (int rt = 0; rt < kRT; ++rt)
+                xq[rt] = *reinterpret_cast<const uint4*>(base + (size_t)(kRT * warp + rt) * RP);
 #pragma unroll
-        for (int re = 0; re < RE; ++re) {
-            float wv[8];
-            load8(base + (size_t)(kTok + re) * RP, wv, (T*)nullptr);
+            for (int re = 0; re < RE; ++re) {
+                const uint4 wq = *reinterpret_cast<const uint4*>(base + (size_t)(kTok + re) * RP);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+                for (int rt = 0; rt < kRT; ++rt) fma8_bf16(acc[rt * RE + re], xq[rt], wq);
+            }
+        } else {
+            float xv[kRT][8];
 #pragma unroll
-                for (int rt = 0; rt < kRT; ++rt) acc[rt * RE + re] = fmaf(xv[rt][j], wv[j], acc[rt * RE + re]);
+            for (int rt = 0; rt < kRT; ++rt) load8(base + (size_t)(kRT * warp + rt) * RP, xv[rt], (T*)nullptr);
+#pragma unroll
+            for (int re = 0; re < RE; ++re) {
+                float wv[8];
+                load8(base + (size_t)(kTok + re) * RP, wv, (T*)nullptr);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int rt = 0; rt < kRT; ++rt)
+                        acc[rt * RE + re] = fmaf(xv[rt][j], wv[j], acc[rt * RE + re]);
+            }
         }
         const int pass = q / nchunks;
         if (q - pass * nchunks == nchunks - 1) {
@@ -234,16 +279,20 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     const int kr = fb_idx ? 2 * k : k;  // ranks selected: the choices, then the fallbacks
 
     if (E <= 32) {
-        // softmax + top-k: one thread per token
-        if (tid < kTok && t0 + tid < T_) {
+        // softmax + top-k: one thread per token, warp 0 (rows of tokens past T
+        // hold bias-only logits and write nothing); a rank's per-expert counts
+        // for the block come from one warp match, stored by each group's
+        // first lane (no shared-memory atomics)
+        if (tid < kTok) {
             const int64_t t = t0 + tid;
+            const bool valid = t < T_;
             const float* gl = lg + tid * LGP;
             float m = -CUDART_INF_F;
             for (int e = 0; e < E; ++e) m = fmaxf(m, gl[e]);
             float s = 0.0f;
             for (int e = 0; e < E; ++e) s += expf(gl[e] - m);
             const float inv = 1.0f / s;
-            if (probs)
+            if (probs && valid)
                 for (int e = 0; e < E; ++e) probs[(size_t)t * E + e] = expf(gl[e] - m) * inv;
             uint32_t taken = 0;
             float chosen[8];
@@ -259,15 +308,21 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
                 }
                 taken |= 1u << be;
                 if (r >= k) {
-                    fb_idx[(size_t)t * k + r - k] = be;
-                    if (fb_gate) fb_gate[(size_t)t * k + r - k] = expf(bv - m) * inv;
+                    if (valid) {
+                        fb_idx[(size_t)t * k + r - k] = be;
+                        if (fb_gate) fb_gate[(size_t)t * k + r - k] = expf(bv - m) * inv;
+                    }
                     continue;
                 }
                 chosen[r] = bv;
-                if (topk_idx) topk_idx[(size_t)t * k + r] = be;
-                if (count) atomicAdd(&cnt[r * E + be], 1);
+                if (valid && topk_idx) topk_idx[(size_t)t * k + r] = be;
+                if (count) {
+                    const int key = valid ? be : -1;
+                    const uint32_t same = __match_any_sync(0xffffffffu, key);
+                    if (valid && tid == __ffs(same) - 1) cnt[r * E + be] = __popc(same);
+                }
             }
-            if (topk_gate) write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
+            if (valid && topk_gate) write_gates(topk_gate + (size_t)t * k, chosen, k, m, inv, renorm);
         }
     } else {
         // softmax + top-k: one warp per token, lane holds experts lane + 32 q
