@@ -192,7 +192,7 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
     if (ec) {
         // expert choice: router logits and probabilities, then each expert
         // takes its tokens by logit
-        e = launch_route(p, x, Wg, bias, nullptr, nullptr, probs, s, logits);
+        e = launch_route(p, x, Wg, bias, nullptr, nullptr, probs, s, logits, nullptr, nullptr, status);
         if (e == cudaSuccess) e = launch_ec_select(p, logits, row_token, off, sel_row, s);
     } else {
         // router + count pass (status[1] is the count pass's completion ticket), then the rank pass
@@ -205,14 +205,14 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
             // (final experts and gates overwrite idx and gate in place)
             int32_t* fb_idx = (int32_t*)(w + L.fallback_idx);
             float* fb_gate = (float*)(w + L.fallback_gate);
-            e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s, fb_idx, fb_gate);
+            e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s, fb_idx, fb_gate, status);
             AssignScan second = scan;
             second.second = true;
             second.rerouted = (int32_t*)(w + L.rerouted);
             if (e == cudaSuccess)
                 e = launch_reroute(p, idx, gate, fb_idx, fb_gate, idx, gate, slot, second, row_token, status, s);
         } else {
-            e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s);
+            e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s, nullptr, nullptr, status);
             if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
         }
     }

@@ -2,6 +2,7 @@
 // vector loads, device status bits and the internal launcher declarations.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -132,10 +133,11 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 
 // ---- launchers (each returns cudaGetLastError() of its launches) ----------
 // logits (optional): the fp32 router logits [T, E], bias included
+// status (optional): the workspace's status word, for a copy that never lands
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
                          int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s,
                          float* logits = nullptr, int32_t* fallback_idx = nullptr,
-                         float* fallback_gate = nullptr);
+                         float* fallback_gate = nullptr, int* status = nullptr);
 
 // router plus the count pass of the slot assignment (hist and scan outputs in
 // `scan`, defined in assign_scan.cuh); T must be > 0
@@ -145,7 +147,7 @@ struct AssignScan;
 cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
                                int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
                                cudaStream_t s, int32_t* fallback_idx = nullptr,
-                               float* fallback_gate = nullptr);
+                               float* fallback_gate = nullptr, int* status = nullptr);
 
 cudaError_t launch_assign(const Problem& p, const int32_t* topk_idx, int32_t* slot_pos,
                           int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
@@ -196,6 +198,12 @@ cudaError_t launch_ec_combine(const Problem& p, const void* yd, const float* pro
 cudaError_t launch_ffn_simt(const Problem& p, const void* xd, const int32_t* expert_offsets,
                             const void* W1, const void* W3, const void* W2, void* h, void* yd,
                             cudaStream_t s);
+
+// Tensor map of a row-major [rows, cols] matrix (bf16 or fp32) for unswizzled
+// TMA tile loads of box_rows x box_cols; out-of-range elements read as zero.
+// False when the encoder is unavailable or rejects the arguments.
+bool encode_row_tiles(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                      uint32_t box_rows);
 
 // tcgen05 grouped GEMM path (bf16 + SwiGLU). Returns cudaErrorNotSupported
 // when the tensor-map encoder cannot be obtained.

@@ -638,6 +638,25 @@ bool make_map(EncodeTiledFn enc, CUtensorMap* m, const void* base, uint64_t rows
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool encode_row_tiles(CUtensorMap* m, const void* base, int dtype, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                      uint32_t box_rows) {
+    EncodeTiledFn enc = get_encoder();
+    if (!enc) return false;
+    const uint64_t eb = dtype == MOE_BF16 ? 2 : 4;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * eb};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(m, dtype == MOE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 int num_sms() {
     static int n = 0;
     if (n == 0) {

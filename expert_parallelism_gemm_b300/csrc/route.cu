@@ -20,9 +20,12 @@
 // 4*RE (token, expert) pairs, so each lane keeps 4*RE slice sums and every
 // 16-byte shared-memory load feeds 8*RE (x row) or 32 (Wg row) multiply-adds
 // per lane.  The hidden dimension is walked in
-// chunks of 256 elements (8 per lane) through an S-stage ring of cp.async
-// copies (32 x rows and the pass's 8 Wg rows, in their storage type,
-// zero-filled past T, E and d; a zero element adds an exact zero product).
+// chunks of 256 elements (8 per lane) through an S-stage ring of TMA tile
+// copies: per chunk one thread issues two 2-D box loads (the CTA's 32 x rows
+// and the pass's RE Wg rows, in their storage type, zero-filled past T, E and
+// d -- a zero element adds an exact zero product) that complete on the
+// stage's mbarrier.  Every wait on a stage is bounded in time; on expiry the
+// kernel records MOE_ERR_TIMEOUT's device bit and stops computing.
 // After the last chunk of a pass the warp reduces its pairs with the
 // butterfly in reduce-scatter form: in round o a lane keeps the half of its
 // pairs selected by bit o of its lane index and adds the partner's copy of
@@ -56,14 +59,44 @@ constexpr int kKC = 256;                     // hidden elements per chunk (32 la
 static_assert(kTok == kAssignBlock, "one CTA per assignment block");
 static_assert(kRouteThreads / 32 * kRT == kTok, "warp tiles cover the CTA's tokens");
 
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g), "r"(src_bytes)
+constexpr uint64_t kRouteTimeoutNs = 2000000000ull;  // 2 s: far above any legitimate wait
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t route_timer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait for the phase of `parity`; false after kRouteTimeoutNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = route_timer();
+    while (!mbar_try_wait(bar, parity))
+        if (route_timer() - t0 > kRouteTimeoutNs) return false;
+    return true;
+}
+// 2-D box of `map` at (c0 = column, c1 = row) into shared memory at dst.
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
 }
 
 // 8 consecutive elements of a shared-memory row, widened to fp32.
@@ -138,29 +171,30 @@ constexpr int route_stages_small_e() {
 template <int RE>
 size_t route_smem_bytes(int elem_bytes, int stages, int E, int k) {
     const int epad = (E + RE - 1) / RE * RE;
-    return (size_t)stages * (kTok + RE) * kKC * elem_bytes + (size_t)kTok * (epad + 1) * sizeof(float) +
+    return 128 + (size_t)stages * (kTok + RE) * kKC * elem_bytes + (size_t)kTok * (epad + 1) * sizeof(float) +
            (size_t)k * E * sizeof(int);
 }
 
 template <typename T, int RE, int S>
-__global__ void __launch_bounds__(kRouteThreads)
-route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* __restrict__ Wg,
-             const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
+__global__ void __launch_bounds__(kRouteThreads, 2)
+route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, int64_t T_, int d,
+             int E, int k, const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
              float* __restrict__ topk_gate, float* __restrict__ probs, float* __restrict__ logits,
-             int32_t* __restrict__ fb_idx, float* __restrict__ fb_gate, const int renorm,
+             int32_t* __restrict__ fb_idx, float* __restrict__ fb_gate, const int renorm, int* status,
              const AssignScan scan) {
-    constexpr int VE = vec_elems<T>();               // elements per 16-byte vector
     constexpr int RP = kKC * (int)sizeof(T);         // ring row pitch, bytes
-    constexpr int VPR = RP / 16;                     // 16-byte vectors per ring row
     constexpr int kStageRows = kTok + RE;            // x rows, then the pass's Wg rows
+    constexpr uint32_t kStageBytes = (uint32_t)kStageRows * RP;
     constexpr int NP = kRT * RE;                     // (token, expert) pairs per warp
     constexpr int PL = NP / 32;                      // pairs per lane after the butterfly
 
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint8_t* ring = smem;  // [S][kStageRows][RP]
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[S];        // one per ring stage: the stage's copies landed
+    const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    uint8_t* ring = smem_raw + ((128u - (raw_s & 127u)) & 127u);  // [S][kStageRows][RP], TMA-aligned
     const int npass = (E + RE - 1) / RE;
     const int LGP = npass * RE + 1;
-    float* lg = reinterpret_cast<float*>(smem + (size_t)S * kStageRows * RP);  // [kTok][LGP]
+    float* lg = reinterpret_cast<float*>(ring + (size_t)S * kStageRows * RP);  // [kTok][LGP]
     int* cnt = reinterpret_cast<int*>(lg + kTok * LGP);                         // [k][E]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -168,58 +202,48 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
     const int nchunks = (d + kKC - 1) / kKC;
     const int nq = npass * nchunks;
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+    const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(bars);
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(bar_s + 8u * i, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
     dep_wait();
     dep_release();
 
-    // copies of flattened chunk q = (pass, chunk) into ring slot q % S; always
-    // commits a group.  Thread tid copies the 16-byte column colv of rows
-    // row0, row0 + RPI, ...: the first kTok / RPI of them x rows (token
-    // pointers fixed for the CTA), the rest the pass's Wg rows.
-    constexpr int RPI = kRouteThreads / VPR;  // rows per sweep of the CTA's threads
-    constexpr int NX = kTok / RPI, NI = kStageRows / RPI;
-    static_assert(kTok % RPI == 0 && kStageRows % RPI == 0, "rows split evenly over the threads");
-    const int row0 = tid / VPR, colv = (tid % VPR) * VE;
-    const T* xrow[NX];
-#pragma unroll
-    for (int i = 0; i < NX; ++i) {
-        const int64_t t = t0 + row0 + RPI * i;
-        xrow[i] = t < T_ ? x + (size_t)t * d + colv : nullptr;
-    }
+    // thread 0 loads flattened chunk q = (pass, chunk) into ring slot q % S:
+    // the CTA's x rows and the pass's Wg rows, one box each
+    int issued = 0;
     auto issue = [&](int q) {
         if (q < nq) {
             const int pass = q / nchunks, c = q - pass * nchunks;
-            const int k0 = c * kKC;
-            const bool in_d = k0 + colv < d;  // d is a multiple of VE
-            const uint32_t slot =
-                ring_s + (uint32_t)((q % S) * kStageRows * RP + colv * (int)sizeof(T) + row0 * RP);
-#pragma unroll
-            for (int i = 0; i < NX; ++i) {
-                const bool ok = in_d && xrow[i] != nullptr;
-                cp_async16(slot + (uint32_t)(RPI * i * RP), ok ? (const void*)(xrow[i] + k0) : (const void*)x,
-                           ok ? 16u : 0u);
-            }
-#pragma unroll
-            for (int i = NX; i < NI; ++i) {
-                const int e = pass * RE + row0 + RPI * i - kTok;
-                const bool ok = in_d && e < E;
-                cp_async16(slot + (uint32_t)(RPI * i * RP), Wg + (ok ? (size_t)e * d + k0 + colv : 0),
-                           ok ? 16u : 0u);
-            }
+            const uint32_t slot = ring_s + (uint32_t)(q % S) * kStageBytes;
+            const uint32_t bar = bar_s + 8u * (uint32_t)(q % S);
+            mbar_expect_tx(bar, kStageBytes);
+            tma_box(slot, &tmx, bar, c * kKC, (int)t0);
+            tma_box(slot + (uint32_t)(kTok * RP), &tmw, bar, c * kKC, pass * RE);
+            issued = q + 1;
         }
-        cp_async_commit();
     };
 
     float acc[NP];  // slice sums of pair p = rt * RE + re
 #pragma unroll
     for (int p = 0; p < NP; ++p) acc[p] = 0.0f;
 
-#pragma unroll
-    for (int q = 0; q < S - 1; ++q) issue(q);
-    for (int q = 0; q < nq; ++q) {
-        // committed: chunks 0..q+S-2; chunk q must have landed
-        cp_async_wait<S - 2>();
-        __syncthreads();  // chunk q visible; every thread is done with chunk q-1
-        issue(q + S - 1);  // into the slot chunk q-1 used
+    if (tid == 0)
+        for (int q = 0; q < S - 1; ++q) issue(q);
+    bool aborted = false;
+    int q = 0;
+    for (; q < nq; ++q) {
+        // chunk q must have landed (bounded wait); the barrier also means
+        // every thread is done with chunk q-1, whose slot is refilled next
+        const bool late = !mbar_wait_bounded(bar_s + 8u * (uint32_t)(q % S), (uint32_t)((q / S) & 1));
+        if (late && status) atomicOr(status, kDevTimeout);
+        if (__syncthreads_or(late)) {
+            aborted = true;
+            break;
+        }
+        if (tid == 0) issue(q + S - 1);
         const uint8_t* base = ring + (size_t)(q % S) * kStageRows * RP + lane * 8 * (int)sizeof(T);
         if constexpr (sizeof(T) == 2) {
             uint4 xq[kRT];
@@ -271,7 +295,15 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
             for (int p = 0; p < NP; ++p) acc[p] = 0.0f;
         }
     }
-    cp_async_wait<0>();
+    if (aborted) {
+        // a copy never landed: let thread 0 wait (bounded) for the copies it
+        // issued, and run the rest on zero logits so that every index stays
+        // in range (the status word reports the error)
+        if (tid == 0)
+            for (int c = q; c < issued; ++c)
+                if (!mbar_wait_bounded(bar_s + 8u * (uint32_t)(c % S), (uint32_t)((c / S) & 1))) break;
+        for (int i = tid; i < kTok * LGP; i += kRouteThreads) lg[i] = 0.0f;
+    }
     if (scan.hist)
         for (int i = tid; i < k * E; i += kRouteThreads) cnt[i] = 0;
     __syncthreads();
@@ -408,15 +440,18 @@ route_kernel(int64_t T_, int d, int E, int k, const T* __restrict__ x, const T* 
 template <typename T, int RE, int S>
 cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, const float* bias,
                             int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
-                            int32_t* fb_idx, float* fb_gate, const AssignScan& scan, cudaStream_t s) {
+                            int32_t* fb_idx, float* fb_gate, int* status, const AssignScan& scan, cudaStream_t s) {
+    CUtensorMap tmx, tmw;
+    if (!encode_row_tiles(&tmx, x, p.dtype, (uint64_t)p.T, (uint64_t)p.d, kKC, kTok) ||
+        !encode_row_tiles(&tmw, Wg, p.dtype, (uint64_t)p.E, (uint64_t)p.d, kKC, RE))
+        return cudaErrorInvalidValue;
     const size_t smem = route_smem_bytes<RE>((int)sizeof(T), S, p.E, p.k);
     auto kern = route_kernel<T, RE, S>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const unsigned grid = (unsigned)ceil_div(p.T, kTok);
-    return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, p.T, p.d, p.E, p.k, (const T*)x,
-                    (const T*)Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx, fb_gate,
-                    (int)(p.flags & MOE_FLAG_RENORM), scan);
+    return launch_k(kern, dim3(grid), dim3(kRouteThreads), smem, s, tmx, tmw, p.T, p.d, p.E, p.k, bias, topk_idx,
+                    topk_gate, probs, logits, fb_idx, fb_gate, (int)(p.flags & MOE_FLAG_RENORM), status, scan);
 }
 
 // 16 experts per pass for 9..64 experts (measured faster at 64), 8 otherwise
@@ -424,40 +459,41 @@ cudaError_t launch_route_re(const Problem& p, const void* x, const void* Wg, con
 template <typename T>
 cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, const float* bias,
                            int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
-                           int32_t* fb_idx, float* fb_gate, const AssignScan& scan, cudaStream_t s) {
+                           int32_t* fb_idx, float* fb_gate, int* status, const AssignScan& scan,
+                           cudaStream_t s) {
     if (p.E <= 8)
         return launch_route_re<T, 8, route_stages_small_e<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits,
-                                                                fb_idx, fb_gate, scan, s);
+                                                                fb_idx, fb_gate, status, scan, s);
     if (p.E <= 64)
         return launch_route_re<T, 16, route_stages<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits,
-                                                         fb_idx, fb_gate, scan, s);
+                                                         fb_idx, fb_gate, status, scan, s);
     return launch_route_re<T, 8, route_stages<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fb_idx,
-                                                    fb_gate, scan, s);
+                                                    fb_gate, status, scan, s);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const float* bias,
                          int32_t* topk_idx, float* topk_gate, float* probs, cudaStream_t s, float* logits,
-                         int32_t* fallback_idx, float* fallback_gate) {
+                         int32_t* fallback_idx, float* fallback_gate, int* status) {
     if (p.T == 0) return cudaSuccess;
     AssignScan none{};
     if (p.dtype == MOE_BF16)
         return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fallback_idx,
-                                             fallback_gate, none, s);
+                                             fallback_gate, status, none, s);
     return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fallback_idx, fallback_gate,
-                                 none, s);
+                                 status, none, s);
 }
 
 cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, const float* bias,
                                int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
-                               cudaStream_t s, int32_t* fallback_idx, float* fallback_gate) {
+                               cudaStream_t s, int32_t* fallback_idx, float* fallback_gate, int* status) {
     if (p.T == 0) return cudaErrorInvalidValue;  // callers handle T = 0 without a launch
     if (p.dtype == MOE_BF16)
         return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, fallback_idx,
-                                             fallback_gate, scan, s);
+                                             fallback_gate, status, scan, s);
     return launch_route_t<float>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, fallback_idx,
-                                 fallback_gate, scan, s);
+                                 fallback_gate, status, scan, s);
 }
 
 }  // namespace moe
