@@ -24,8 +24,11 @@
 // copies: per chunk one thread issues two 2-D box loads (the CTA's 32 x rows
 // and the pass's RE Wg rows, in their storage type, zero-filled past T, E and
 // d -- a zero element adds an exact zero product) that complete on the
-// stage's mbarrier.  Every wait on a stage is bounded in time; on expiry the
-// kernel records MOE_ERR_TIMEOUT's device bit and stops computing.
+// stage's "full" mbarrier; each warp, done with a chunk, arrives on the
+// stage's "empty" mbarrier, and only the issuing thread waits on that before
+// refilling the stage (no CTA-wide barrier per chunk).  Every wait is bounded
+// in time; on expiry the kernel records MOE_ERR_TIMEOUT's device bit and
+// stops computing.
 // After the last chunk of a pass the warp reduces its pairs with the
 // butterfly in reduce-scatter form: in round o a lane keeps the half of its
 // pairs selected by bit o of its lane index and adds the partner's copy of
@@ -83,12 +86,23 @@ __device__ __forceinline__ uint64_t route_timer() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Bounded wait for the phase of `parity`; false after kRouteTimeoutNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// Wait for the phase of `parity`.  Gives up (false) when *abort is raised or
+// after kRouteTimeoutNs, then raising *abort and recording the timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = route_timer();
-    while (!mbar_try_wait(bar, parity))
-        if (route_timer() - t0 > kRouteTimeoutNs) return false;
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (route_timer() - t0 > kRouteTimeoutNs) {
+            *abort = 1;
+            if (status) atomicOr(status, kDevTimeout);
+            return false;
+        }
+    }
     return true;
 }
 // 2-D box of `map` at (c0 = column, c1 = row) into shared memory at dst.
@@ -189,7 +203,8 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
     constexpr int PL = NP / 32;                      // pairs per lane after the butterfly
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[S];        // one per ring stage: the stage's copies landed
+    __shared__ __align__(8) uint64_t bars[2 * S];    // per stage: copies landed ("full"), warps done ("empty")
+    __shared__ int s_abort;
     const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(smem_raw);
     uint8_t* ring = smem_raw + ((128u - (raw_s & 127u)) & 127u);  // [S][kStageRows][RP], TMA-aligned
     const int npass = (E + RE - 1) / RE;
@@ -203,8 +218,14 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
     const int nq = npass * nchunks;
     const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
     const uint32_t bar_s = (uint32_t)__cvta_generic_to_shared(bars);
+    const uint32_t empty_s = bar_s + 8u * S;
+    volatile int* abort_flag = &s_abort;
     if (tid == 0) {
-        for (int i = 0; i < S; ++i) mbar_init(bar_s + 8u * i, 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(bar_s + 8u * i, 1);
+            mbar_init(empty_s + 8u * i, kRouteThreads / 32);
+        }
+        s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -232,18 +253,19 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
 
     if (tid == 0)
         for (int q = 0; q < S - 1; ++q) issue(q);
-    bool aborted = false;
-    int q = 0;
-    for (; q < nq; ++q) {
-        // chunk q must have landed (bounded wait); the barrier also means
-        // every thread is done with chunk q-1, whose slot is refilled next
-        const bool late = !mbar_wait_bounded(bar_s + 8u * (uint32_t)(q % S), (uint32_t)((q / S) & 1));
-        if (late && status) atomicOr(status, kDevTimeout);
-        if (__syncthreads_or(late)) {
-            aborted = true;
-            break;
+    for (int q = 0; q < nq; ++q) {
+        // thread 0 refills the stage of chunk q-1 with chunk q+S-1 once every
+        // warp is done with chunk q-1 (stage S-1 is still unused at q = 0)
+        if (tid == 0 && q + S - 1 < nq) {
+            if (q == 0 || mbar_wait_bounded(empty_s + 8u * (uint32_t)((q - 1) % S),
+                                            (uint32_t)(((q - 1) / S) & 1), abort_flag, status))
+                issue(q + S - 1);
         }
-        if (tid == 0) issue(q + S - 1);
+        // the warp leaves together (its lanes meet again in shuffles) if any
+        // lane's wait gave up
+        const bool landed =
+            mbar_wait_bounded(bar_s + 8u * (uint32_t)(q % S), (uint32_t)((q / S) & 1), abort_flag, status);
+        if (!__all_sync(0xffffffffu, landed)) break;
         const uint8_t* base = ring + (size_t)(q % S) * kStageRows * RP + lane * 8 * (int)sizeof(T);
         if constexpr (sizeof(T) == 2) {
             uint4 xq[kRT];
@@ -271,6 +293,8 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
                         acc[rt * RE + re] = fmaf(xv[rt][j], wv[j], acc[rt * RE + re]);
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_s + 8u * (uint32_t)(q % S));  // this warp is done with the stage
         const int pass = q / nchunks;
         if (q - pass * nchunks == nchunks - 1) {
             // end of a pass: butterfly in reduce-scatter form, lane j gets
@@ -295,13 +319,18 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
             for (int p = 0; p < NP; ++p) acc[p] = 0.0f;
         }
     }
-    if (aborted) {
-        // a copy never landed: let thread 0 wait (bounded) for the copies it
-        // issued, and run the rest on zero logits so that every index stays
-        // in range (the status word reports the error)
-        if (tid == 0)
-            for (int c = q; c < issued; ++c)
-                if (!mbar_wait_bounded(bar_s + 8u * (uint32_t)(c % S), (uint32_t)((c / S) & 1))) break;
+    __syncthreads();
+    if (s_abort) {
+        // a wait gave up: thread 0 waits (bounded) for the copies that may
+        // still be in flight -- the last S-1 it issued, each in its own stage
+        // -- and the rest runs on zero logits so that every index stays in
+        // range (the status word reports the error)
+        if (tid == 0) {
+            int quiet = 0;
+            for (int c = issued - (S - 1) > 0 ? issued - (S - 1) : 0; c < issued; ++c)
+                if (!mbar_wait_bounded(bar_s + 8u * (uint32_t)(c % S), (uint32_t)((c / S) & 1), &quiet, status))
+                    break;
+        }
         for (int i = tid; i < kTok * LGP; i += kRouteThreads) lg[i] = 0.0f;
     }
     if (scan.hist)
