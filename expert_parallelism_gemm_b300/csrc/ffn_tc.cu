@@ -611,18 +611,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
                                   CUtensorMapFloatOOBfill);
 
+// Looked up once per process (a function-local static: thread-safe).
 EncodeTiledFn get_encoder() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiledFn)ptr;
-    }
+            return (EncodeTiledFn)ptr;
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -657,13 +656,15 @@ bool encode_row_tiles(CUtensorMap* m, const void* base, int dtype, uint64_t rows
 
 namespace {
 
+// Both queries below run once per process (function-local statics, so
+// thread-safe); every device the library drives is the same part.
 int num_sms() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
+    static const int n = []() {
+        int dev = 0, v = 0;
         cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    }
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        return v;
+    }();
     return n;
 }
 
@@ -689,8 +690,7 @@ cudaError_t launch_pairs(void (*kern)(KArgs...), unsigned clusters, cudaStream_t
 
 // Clusters of two that can be resident at once (one CTA per SM).
 int max_pairs() {
-    static int n = 0;
-    if (n == 0) {
+    static const int n = []() {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(num_sms() / kCluster * kCluster));
         cfg.blockDim = dim3(kTcThreads);
@@ -705,8 +705,8 @@ int max_pairs() {
         int c = 0;
         if (cudaOccupancyMaxActiveClusters(&c, tc_ffn_kernel, &cfg) != cudaSuccess || c <= 0)
             c = num_sms() / kCluster;
-        n = c;
-    }
+        return c;
+    }();
     return n;
 }
 
@@ -729,13 +729,9 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
         !make_map(enc, &mB2, W2, E * p.d, p.ffn, BN / 2))
         return cudaErrorInvalidValue;
 
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e1 =
-            cudaFuncSetAttribute(tc_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e1 != cudaSuccess) return e1;
-        attr_done = true;
-    }
+    // per device, so set on every launch (a cheap host call)
+    cudaError_t e1 = cudaFuncSetAttribute(tc_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e1 != cudaSuccess) return e1;
     // upper bound of m-tile pairs over all experts: sum_e ceil(mt_e / 2) with
     // mt_e = ceil(n_e / BM), n_e <= C, sum_e mt_e <= ceil(rows_max / BM) + E
     const int64_t mp_cap = ceil_div(ceil_div(p.C, BM), 2);

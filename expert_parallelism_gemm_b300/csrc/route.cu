@@ -113,10 +113,8 @@ __device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, ui
         : "memory");
 }
 
-// 8 consecutive elements of a shared-memory row, widened to fp32.
-__device__ __forceinline__ void load8(const uint8_t* p, float (&v)[8], __nv_bfloat16*) {
-    unpack(*reinterpret_cast<const Vec16*>(p), v, (__nv_bfloat16*)nullptr);
-}
+// 8 consecutive fp32 elements of a shared-memory row (the fp32 router; the
+// bf16 one feeds its packed halves to fma8_bf16 instead).
 __device__ __forceinline__ void load8(const uint8_t* p, float (&v)[8], float*) {
     const float4 a = *reinterpret_cast<const float4*>(p);
     const float4 b = *reinterpret_cast<const float4*>(p + 16);
