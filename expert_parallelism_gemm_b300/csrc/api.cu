@@ -189,6 +189,7 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
     float* logits = (float*)(w + L.logits);
     int32_t* sel_row = (int32_t*)(w + L.sel_row);
     cudaError_t e;
+    bool packed = false;  // slot assignment and dispatch done by one kernel
     if (ec) {
         // expert choice: router logits and probabilities, then each expert
         // takes its tokens by logit
@@ -211,12 +212,19 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
             second.rerouted = (int32_t*)(w + L.rerouted);
             if (e == cudaSuccess)
                 e = launch_reroute(p, idx, gate, fb_idx, fb_gate, idx, gate, slot, second, row_token, status, s);
+        } else if (assign_pack_fits(p)) {
+            // small histogram: the router only counts; one kernel scans, places and packs
+            AssignScan deferred = scan;
+            deferred.defer = true;
+            e = launch_route_count(p, x, Wg, bias, idx, gate, deferred, s, nullptr, nullptr, status);
+            if (e == cudaSuccess) e = launch_assign_pack(p, x, idx, scan, slot, row_token, xd, status, s);
+            packed = true;
         } else {
             e = launch_route_count(p, x, Wg, bias, idx, gate, scan, s, nullptr, nullptr, status);
             if (e == cudaSuccess) e = launch_rank(p, idx, hist, off, slot, row_token, status, s);
         }
     }
-    if (e == cudaSuccess) e = launch_dispatch(p, x, row_token, off, xd, s);
+    if (e == cudaSuccess && !packed) e = launch_dispatch(p, x, row_token, off, xd, s);
     if (e == cudaSuccess) {
         if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
             e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, (int*)(w + L.ffn_sync), s);

@@ -42,6 +42,7 @@ struct AssignScan {
     int64_t nblk, C, C_shard;
     int32_t* rerouted = nullptr;  // second pass only; may be null
     bool second = false;
+    bool defer = false;  // the router writes the histogram only; a later kernel scans it
 };
 
 // Call from every thread of every CTA after the CTA's hist entries are

@@ -168,6 +168,13 @@ cudaError_t launch_reroute(const Problem& p, const int32_t* topk_idx, const floa
                            float* route_gate, int32_t* slot_pos, const AssignScan& second, int32_t* row_token,
                            int* status, cudaStream_t s);
 
+// slot positions, scan outputs and the pack in one kernel, after a router
+// launch that wrote the histogram with scan.defer set; for problems where
+// assign_pack_fits() holds
+bool assign_pack_fits(const Problem& p);
+cudaError_t launch_assign_pack(const Problem& p, const void* x, const int32_t* topk_idx, const AssignScan& a,
+                               int32_t* slot_pos, int32_t* row_token, void* xd, int* status, cudaStream_t s);
+
 // rank pass alone (the histogram already holds the scanned prefixes)
 cudaError_t launch_rank(const Problem& p, const int32_t* topk_idx, const int32_t* hist,
                         const int32_t* expert_offsets, int32_t* slot_pos, int32_t* row_token, int* status,

@@ -45,9 +45,11 @@
 //
 // Inside the layer forward the router also starts the slot assignment: a CTA
 // holds exactly one assignment block of kAssignBlock tokens, so it counts its
-// tokens' rank-r choices per expert (shared-memory integer counts), writes
-// that block's histogram entries, and the last CTA to finish scans them
-// (assign_scan.cuh).  The standalone router call leaves this out.
+// tokens' rank-r choices per expert (one warp match per rank), writes that
+// block's histogram entries, and the last CTA to finish scans them
+// (assign_scan.cuh) -- or, when the histogram is small, leaves the scan to the
+// fused slot-and-pack kernel (assign_pack.cu).  The standalone router call
+// leaves all of this out.
 #include <math_constants.h>
 
 #include "assign_scan.cuh"
@@ -460,7 +462,7 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
             const int e = i / k, r = i % k;
             scan.hist[((size_t)e * k + r) * scan.nblk + b] = cnt[r * E + e];
         }
-        finish_assign_scan(scan);
+        if (!scan.defer) finish_assign_scan(scan);
     }
 }
 

@@ -212,6 +212,16 @@ def test_layer_forward(case):
     np.testing.assert_array_equal(dev.region("shard_overflow", torch.int32, wl.D).cpu().numpy(),
                                   s.shard_overflow)
     assert int(dev.region("dropped", torch.int32, 1).item()) == s.dropped
+    # the rest of the slot outputs and the packed rows (written by the fused
+    # slot-and-pack kernel on small histograms, by rank + dispatch otherwise)
+    for f, n in (("counts_routed", wl.E), ("counts_kept", wl.E), ("shard_offsets", wl.D + 1),
+                 ("shard_routed", wl.D)):
+        np.testing.assert_array_equal(dev.region(f, torch.int32, n).cpu().numpy(), getattr(s, f), err_msg=f)
+    kept = int(s.expert_offsets[-1])
+    np.testing.assert_array_equal(dev.region("row_token", torch.int32, kept).cpu().numpy(), s.row_token)
+    if kept:
+        xd_ws = dev.region("xd", dev.dtype, kept * wl.d).view(kept, wl.d)
+        np.testing.assert_array_equal(raw(xd_ws), o["xd"])
     if name in SMALL:
         yd_o = oracle.expert_ffn(o["xd"], s.expert_offsets, cpu.W1, cpu.W3, cpu.W2, act)
         want = oracle.combine(yd_o, o["idx"], s.slot_pos, o["gate"], s.expert_offsets, resid,
