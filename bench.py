@@ -537,8 +537,9 @@ def cpu_baseline(wl, budget_s=12.0):
             break
     return {"value": oracle_tokens_per_s(wl, r_s, s_s, n), "unit": "tokens/s", "cores": oracle_cores(),
             "kind": "oracle",
-            "sample": f"routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random tokens, "
-                      f"extrapolated to {wl.T} ({r_s + s_s:.1f} s of CPU work)"}
+            "sample": (f"the whole layer, all {wl.T} tokens ({r_s + s_s:.1f} s of CPU work)" if n >= wl.T else
+                       f"routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random tokens, "
+                       f"extrapolated to {wl.T} ({r_s + s_s:.1f} s of CPU work)")}
 
 
 def run_reference(args, rank):
