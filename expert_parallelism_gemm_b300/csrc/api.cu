@@ -632,7 +632,7 @@ const char* moe_status_string(int status) {
     switch (status) {
         case MOE_OK: return "ok";
         case MOE_ERR_INVALID_ARG: return "invalid argument";
-        case MOE_ERR_UNSUPPORTED: return "unsupported problem for this build";
+        case MOE_ERR_UNSUPPORTED: return "valid problem outside what this library supports";
         case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_TIMEOUT: return "a kernel's bounded wait timed out";

@@ -99,7 +99,7 @@ typedef struct {
 enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1, /* a size, pointer, alignment or limit is wrong  */
-    MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what this build supports   */
+    MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what this library supports */
     MOE_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
     MOE_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed             */
     MOE_ERR_TIMEOUT = 5,     /* a kernel's bounded wait gave up (device word) */
