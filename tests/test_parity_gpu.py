@@ -57,6 +57,13 @@ SMALL = {
                             capacity_factor=1.0, dtype="f32", act="swiglu", seed=20),
     "bf16_gelu": Workload("bf16_gelu", T=200, d=64, E=8, D=4, k=2, ffn=96, capacity_factor=1.0,
                           dtype="bf16", act="gelu", seed=21),
+    # the layer forward's slot-and-pack kernel at its size limit (E*k*ceil(T/32)
+    # = 16384 histogram entries, 64 KB of shared memory), and one block past
+    # it, where the last-CTA scan, rank pass and dispatch run instead
+    "pack_limit": Workload("pack_limit", T=8192, d=64, E=64, D=8, k=1, ffn=64, capacity_factor=1.0,
+                           seed=23, zipf_s=1.0),
+    "pack_limit_plus1": Workload("pack_limit_plus1", T=8224, d=64, E=64, D=8, k=1, ffn=64,
+                                 capacity_factor=1.0, seed=24, zipf_s=1.0),
 }
 FULL = {n: w for n, w in moe_inputs.WORKLOADS.items() if n != "tiny_fp32"}
 
