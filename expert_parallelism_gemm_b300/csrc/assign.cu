@@ -70,7 +70,6 @@ __global__ void __launch_bounds__(kThreads)
 count_kernel(int64_t T, int E, int k, int64_t nblk, const int32_t* __restrict__ idx, AssignScan a,
              int* status) {
     dep_wait();
-    dep_release();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int r = blockIdx.y;
@@ -89,7 +88,6 @@ rank_kernel(int64_t T, int E, int k, int64_t nblk, int64_t C, const int32_t* __r
             const int32_t* __restrict__ hist, const int32_t* __restrict__ expert_offsets,
             int32_t* __restrict__ slot_pos, int32_t* __restrict__ row_token, int* status) {
     dep_wait();
-    dep_release();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int r = blockIdx.y;
@@ -115,7 +113,6 @@ reroute_kernel(int64_t T, int E, int k, int64_t nblk, int64_t C, const int32_t* 
                const int32_t* __restrict__ fb_idx, const float* __restrict__ fb_gate, int32_t* route_idx,
                float* route_gate, int32_t* __restrict__ slot_pos, AssignScan a, int* status) {
     dep_wait();
-    dep_release();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     if (b < nblk) {
@@ -173,7 +170,6 @@ place_kernel(int64_t T, int k, int64_t nblk, int64_t C, int64_t rows_max, const 
              const int32_t* __restrict__ hist, const int32_t* __restrict__ expert_offsets,
              int32_t* __restrict__ slot_pos, int32_t* __restrict__ row_token, int* status) {
     dep_wait();
-    dep_release();
     const int lane = threadIdx.x & 31;
     const int64_t b = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int r = blockIdx.y;

@@ -43,7 +43,6 @@ assign_pack_kernel(int64_t Tn, int d, const T* __restrict__ x, const int32_t* __
     extern __shared__ int sh[];  // [E * k * nblk] prefixes, then offsets [E + 1], routed [E]
     __shared__ int s_row[kAssignBlock];  // row of each lane's assignment, or -1
     dep_wait();
-    dep_release();
     const int E = a.E, k = a.k;
     const int64_t nblk = a.nblk;
     const int64_t L = (int64_t)k * nblk, n = (int64_t)E * L;

@@ -71,7 +71,6 @@ __global__ void __launch_bounds__(kEcThreads)
 ec_select_kernel(int64_t T, int E, int64_t Cc, const float* __restrict__ logits, int32_t* __restrict__ row_token,
                  int32_t* __restrict__ sel_row, int32_t* __restrict__ expert_offsets) {
     dep_wait();
-    dep_release();
     extern __shared__ uint32_t keys[];  // [T]
     __shared__ int hist[256];
     __shared__ int scan_sh[33];
@@ -172,7 +171,6 @@ ec_combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restric
                   const float* __restrict__ probs, const int32_t* __restrict__ sel_row,
                   const T* __restrict__ shared, const T* __restrict__ residual, T* __restrict__ y) {
     dep_wait();
-    dep_release();
     constexpr int VE = vec_elems<T>();
     const int nv = d / VE;
     const int lane = threadIdx.x & 31;

@@ -24,7 +24,6 @@ ffn_simt_kernel(int N, int K, int64_t rows_max, const T* __restrict__ A,
                 const int32_t* __restrict__ expert_offsets, const T* __restrict__ B,
                 const T* __restrict__ B3, T* __restrict__ out) {
     dep_wait();
-    dep_release();
     const int e = blockIdx.z;
     // no offsets: one expert whose rows are 0..rows_max-1 (the shared expert)
     const int64_t o0 = expert_offsets ? (int64_t)expert_offsets[e] : 0;

@@ -327,7 +327,6 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
     }
     // global memory only from here on (earlier kernels on the stream are done)
     dep_wait();
-    dep_release();
     if (warp == 0) {
         // expert offsets; they must be non-decreasing within [0, rows_max],
         // otherwise the kernel records kDevBadIndex and computes nothing

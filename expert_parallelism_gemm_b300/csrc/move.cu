@@ -31,7 +31,6 @@ dispatch_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restrict_
                 const int32_t* __restrict__ row_token, const int32_t* __restrict__ expert_offsets,
                 T* __restrict__ xd) {
     dep_wait();
-    dep_release();
     constexpr int VE = vec_elems<T>();
     constexpr int B = 4;  // 16-byte loads in flight per lane before the stores
     // rows past rows_max do not exist in xd; a token id outside [0, T) is skipped
@@ -65,7 +64,6 @@ combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __res
                const int32_t* __restrict__ expert_offsets, const float* __restrict__ topk_gate,
                const T* __restrict__ shared, const T* __restrict__ residual, T* __restrict__ y) {
     dep_wait();
-    dep_release();
     constexpr int VE = vec_elems<T>();
     constexpr int KM = 8 / CB;  // ranks this instantiation handles (k <= KM)
     const int nv = d / VE;

@@ -230,7 +230,6 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
     }
     __syncthreads();
     dep_wait();
-    dep_release();
 
     // thread 0 loads flattened chunk q = (pass, chunk) into ring slot q % S:
     // the CTA's x rows and the pass's Wg rows, one box each

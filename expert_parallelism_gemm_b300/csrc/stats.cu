@@ -47,7 +47,6 @@ stats_kernel(int64_t T, int E, int k, int64_t tb, const float* __restrict__ prob
              unsigned long long* __restrict__ acc, unsigned* ticket, float* __restrict__ out,
              float* __restrict__ mean_prob) {
     dep_wait();
-    dep_release();
     __shared__ unsigned long long sP[256];
     __shared__ unsigned long long sH;
     __shared__ float sTerm[256];
