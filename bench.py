@@ -483,16 +483,9 @@ def run_ours(args, rank, world, local_rank):
 
 
 def launches_per_step(wl) -> int:
-    """Kernels of one moe_layer_forward: router with the fused count pass,
-    then either one slot-and-pack kernel (small histograms, the library's
-    assign_pack_fits rule restated here) or the rank pass and dispatch, the
-    expert FFN (one launch for the tensor-core path, two for the SIMT path),
-    combine."""
-    tc = wl.dtype == "bf16" and wl.act == "swiglu"
-    nblk = -(-wl.T // 32)
-    n = wl.E * wl.k * nblk
-    packed = nblk > 0 and n <= 16384 and n * 4 * nblk * wl.k <= (32 << 20)
-    return 1 + (1 if packed else 2) + (1 if tc else 2) + 1
+    """Kernels of one moe_layer_forward, as the library counts them."""
+    import expert_parallelism_gemm_b300 as moe
+    return moe.moe_layer_launch_count(moe.problem_of(wl))
 
 
 # -------------------------------------------------------------- oracle --

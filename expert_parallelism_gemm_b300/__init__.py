@@ -34,7 +34,7 @@ EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe
            "moe_combine_shared", "moe_layer_forward_shared", "moe_expert_choice_assign",
            "moe_combine_expert_choice", "moe_router_logits", "moe_route_fallback",
            "moe_assign_slots_reroute", "moe_host_alloc", "moe_host_free", "moe_host_staging_size",
-           "moe_layer_forward_host")
+           "moe_layer_forward_host", "moe_layer_launch_count")
 
 
 class moe_problem(ctypes.Structure):
@@ -99,6 +99,7 @@ def load() -> ctypes.CDLL:
     lib.moe_host_free.argtypes = [P]
     lib.moe_host_staging_size.argtypes = [PP, ctypes.POINTER(ctypes.c_size_t)]
     lib.moe_layer_forward_host.argtypes = [PP, ctypes.c_int64, P, P, P, P, P, P, P, P, sz, P, sz, P]
+    lib.moe_layer_launch_count.argtypes = [PP, ctypes.POINTER(ctypes.c_int)]
     lib.moe_status_string.argtypes = [I]
     lib.moe_status_string.restype = ctypes.c_char_p
     for n in EXPORTS:
@@ -336,6 +337,13 @@ def moe_layer_forward_host(problem, x_hosts, Wg, bias, W1, W3, W2, y_hosts, stag
                                          _p(W2), ys, _p(staging), int(staging_bytes), _p(ws), int(ws_bytes),
                                          _stream(stream)),
            "moe_layer_forward_host")
+
+
+def moe_layer_launch_count(problem: moe_problem) -> int:
+    """Kernels one moe_layer_forward launches for this problem (host-only)."""
+    n = ctypes.c_int()
+    _check(load().moe_layer_launch_count(ctypes.byref(problem), ctypes.byref(n)), "moe_layer_launch_count")
+    return n.value
 
 
 def moe_device_status(ws, stream=None) -> int:

@@ -612,6 +612,27 @@ int moe_layer_forward_host(const moe_problem* mp, int64_t n_steps, const void* c
     return MOE_OK;
 }
 
+int moe_layer_launch_count(const moe_problem* mp, int* launches) {
+    if (!launches) return MOE_ERR_INVALID_ARG;
+    Problem p;
+    int rc = to_problem(mp, &p);
+    if (rc != MOE_OK) return rc;
+    if (p.T == 0) {
+        *launches = 0;
+        return MOE_OK;
+    }
+    // the branches of layer_forward: routing and slots, dispatch, FFN(s), combine
+    const int ffn = (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) ? 1 : 2;
+    int n;
+    if (p.flags & MOE_FLAG_EXPERT_CHOICE) n = 2 + 1;        // router, selection; dispatch
+    else if (p.flags & MOE_FLAG_REROUTE) n = 3 + 1;         // router, reroute, place; dispatch
+    else if (assign_pack_fits(p)) n = 2;                    // router, slot-and-pack
+    else n = 2 + 1;                                         // router, rank; dispatch
+    n += ffn + (p.ffn_shared > 0 ? ffn : 0) + 1;            // routed (+ shared) FFN, combine
+    *launches = n;
+    return MOE_OK;
+}
+
 int moe_device_status(void* ws, void* stream) {
     if (!ws) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;

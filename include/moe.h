@@ -421,6 +421,14 @@ int moe_layer_forward_host(const moe_problem* p, int64_t n_steps, const void* co
                            const void* W2, void* const* y_host, void* staging, size_t staging_bytes,
                            void* ws, size_t ws_bytes, void* stream);
 
+/* Number of kernels one moe_layer_forward(_shared) launches for problem *p
+ * (host-only): router and slot assignment (2 when the slot histogram
+ * E*k*ceil(T/32) is small enough for the fused slot-and-pack kernel, else 3
+ * with dispatch; expert choice 3, rerouting 4), the expert FFN (1 launch on
+ * the bf16 SwiGLU tensor-core path, else 2; twice with a shared expert) and
+ * combine.  0 for T == 0. */
+int moe_layer_launch_count(const moe_problem* p, int* launches);
+
 /* Synchronises `stream`, reads the workspace's device status word, clears it
  * and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE (or MOE_ERR_CUDA if
  * the synchronisation itself failed). */

@@ -33,7 +33,7 @@ def _declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
-    assert len(names) == 25, names
+    assert len(names) == 26, names
     assert sorted(moe.EXPORTS) == names
     lib = moe.load()
     for n in names:
@@ -187,6 +187,22 @@ def test_host_path_rejects_bad_arguments_before_any_cuda_call():
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG
     # no steps: nothing to do
     moe.moe_layer_forward_host(p, [], A, None, A, A, A, [], A, stg, A, need, stream=0)
+
+
+def test_layer_launch_count():
+    count = lambda **kw: moe.moe_layer_launch_count(_problem(**kw))
+    # T=128: 4 blocks, small histogram -> router, slot-and-pack, FFN, combine
+    assert count() == 4
+    assert count(dtype="f32", act="gelu") == 5          # two-kernel SIMT FFN
+    assert count(ffn_shared=64) == 5                    # + the shared expert's FFN
+    assert count(expert_choice=True) == 5
+    assert count(reroute=True) == 6
+    assert count(T=0) == 0
+    # the slot-and-pack limit: E*k*ceil(T/32) = 16384 entries, and one block past it
+    assert count(T=8192, E=64, D=8, k=1) == 4
+    assert count(T=8224, E=64, D=8, k=1) == 5
+    # redundant histogram reads above 32 MB take the other path too
+    assert count(T=32768, d=4096, E=8, D=8, k=2, ffn=14336, capacity_factor=math.inf) == 5
 
 
 def test_empty_batch_is_a_no_op():
