@@ -55,3 +55,23 @@ def test_two_gloo_ranks_replicas_and_slowest_rank_time():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(4.25, 1, "cpu") == 4.25
     assert bench.job_tokens_per_s(4096, 1, 20, 4.0) == pytest.approx(4096 * 20 / 4.0e-3)
+
+
+def test_reference_arm_prints_its_contract_line():
+    # the oracle arm on the smallest workload: one JSON line with the keys the
+    # benchmark contract names, and no copies in its e2e object
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_fp32", "--steps",
+                          "1", "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["higher_is_better"] is True and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"]
