@@ -528,11 +528,41 @@ def cpu_baseline(wl, budget_s=12.0):
         r_s, s_s, n = oracle_sample_step(wl, cpu, n_next, rng)
         if r_s + s_s >= 0.5 * budget_s or n >= wl.T:
             break
-    return {"value": oracle_tokens_per_s(wl, r_s, s_s, n), "unit": "tokens/s", "cores": oracle_cores(),
-            "kind": "oracle",
-            "sample": (f"the whole layer, all {wl.T} tokens ({r_s + s_s:.1f} s of CPU work)" if n >= wl.T else
-                       f"routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random tokens, "
-                       f"extrapolated to {wl.T} ({r_s + s_s:.1f} s of CPU work)")}
+    out = {"value": oracle_tokens_per_s(wl, r_s, s_s, n), "unit": "tokens/s", "cores": oracle_cores(),
+           "kind": "oracle",
+           "sample": (f"the whole layer, all {wl.T} tokens ({r_s + s_s:.1f} s of CPU work)" if n >= wl.T else
+                      f"routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random tokens, "
+                      f"extrapolated to {wl.T} ({r_s + s_s:.1f} s of CPU work)")}
+    # the same on one thread, on a smaller sample sized from the run above
+    one = single_thread_oracle(wl, cpu, rng, per_tok=s_s / max(n, 1) * oracle_cores(), budget_s=budget_s / 3)
+    if one is not None:
+        out["single_core"] = one
+    return out
+
+
+def _set_omp_threads(n: int) -> bool:
+    import ctypes.util
+    name = ctypes.util.find_library("gomp") or "libgomp.so.1"
+    try:
+        ctypes.CDLL(name).omp_set_num_threads(int(n))
+        return True
+    except OSError:
+        return False
+
+
+def single_thread_oracle(wl, cpu, rng, per_tok, budget_s):
+    """The oracle's tokens/s on one OpenMP thread (routing + slots of all T
+    tokens, FFN + combine of a sample), or None if the runtime is not found."""
+    if not _set_omp_threads(1):
+        return None
+    try:
+        n1 = int(max(8, min(wl.T, budget_s / max(per_tok, 1e-6))))
+        r_s, s_s, n = oracle_sample_step(wl, cpu, n1, rng)
+    finally:
+        _set_omp_threads(oracle_cores())
+    return {"value": oracle_tokens_per_s(wl, r_s, s_s, n), "unit": "tokens/s", "cores": 1,
+            "sample": f"routing + slots of all {wl.T} tokens, expert FFN + combine of {n} random tokens, "
+                      f"extrapolated to {wl.T} ({r_s + s_s:.1f} s on one thread)"}
 
 
 def run_reference(args, rank):
