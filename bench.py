@@ -623,7 +623,8 @@ def main(argv=None):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     out = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        # the oracle baseline is timed on rank 0 of a one-GPU run only
+        if not args.no_cpu_baseline and world == 1:
             out["cpu_baseline"] = cpu_baseline(moe_inputs.WORKLOADS[args.workload])
         print(json.dumps(out), flush=True)
     if world > 1:
