@@ -18,7 +18,8 @@
 //      histogram into exclusive prefixes in (r, b) order and writes counts,
 //      expert and shard offsets, shard statistics and the dropped total
 //      (assign_scan.cuh).  The layer forward's router writes the histogram
-//      and runs the same scan itself, so it skips this kernel;
+//      and runs the same scan itself, so it skips this kernel (and on small
+//      histograms leaves scan, positions and pack to assign_pack.cu);
 //   2. rank:  one warp per (r, b): pos = prefix + number of lower lanes with
 //      the same expert; writes slot_pos and row_token.
 //
