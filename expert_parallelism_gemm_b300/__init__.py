@@ -34,7 +34,7 @@ EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe
            "moe_combine_shared", "moe_layer_forward_shared", "moe_expert_choice_assign",
            "moe_combine_expert_choice", "moe_router_logits", "moe_route_fallback",
            "moe_assign_slots_reroute", "moe_host_alloc", "moe_host_free", "moe_host_staging_size",
-           "moe_layer_forward_host", "moe_layer_launch_count")
+           "moe_layer_forward_host", "moe_layer_launch_count", "moe_assign_slots_static_status")
 
 
 class moe_problem(ctypes.Structure):
@@ -85,6 +85,7 @@ def load() -> ctypes.CDLL:
     lib.moe_combine.argtypes = [PP, P, P, P, P, P, P, P, P]
     lib.moe_layer_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
     lib.moe_assign_slots_static.argtypes = [PP] + [P] * 11
+    lib.moe_assign_slots_static_status.argtypes = [P]
     lib.moe_device_status.argtypes = [P, P]
     lib.moe_routing_stats.argtypes = [PP, P, P, P, P, P, P, sz, P]
     lib.moe_shared_expert_ffn.argtypes = [PP, P, P, P, P, P, P, sz, P]
@@ -226,6 +227,12 @@ def moe_assign_slots_static(problem, topk_idx, slot_pos, counts_routed, counts_k
                                           _p(shard_offsets), _p(shard_routed), _p(shard_overflow),
                                           _p(row_token), _p(dropped), _stream(stream)),
            "moe_assign_slots_static")
+
+
+def moe_assign_slots_static_status(stream=None) -> int:
+    """Status code of moe_assign_slots_static's device word on the current
+    device (synchronises the stream, then reads and clears it); no raise."""
+    return load().moe_assign_slots_static_status(_stream(stream))
 
 
 def moe_dispatch(problem, x, row_token, expert_offsets, xd, stream=None):

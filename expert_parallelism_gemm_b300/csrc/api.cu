@@ -58,6 +58,8 @@ int validate(const moe_problem* p) {
     return MOE_OK;
 }
 
+}  // namespace
+
 int to_problem(const moe_problem* mp, Problem* p) {
     int rc = validate(mp);
     if (rc != MOE_OK) return rc;
@@ -75,6 +77,8 @@ int to_problem(const moe_problem* mp, Problem* p) {
     p->nblk = ceil_div(p->T, kAssignBlock);
     return MOE_OK;
 }
+
+namespace {
 
 // The shared expert as a problem of its own: one expert whose rows are all T
 // tokens in order, width ffn_shared.

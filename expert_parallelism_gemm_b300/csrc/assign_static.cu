@@ -18,8 +18,16 @@
 //    that first call before any stream capture;
 //  - every call shares the one array: calls whose kernels overlap on the
 //    GPU (different streams, or several host threads) race;
-//  - each call clears the ticket and status words it relies on
-//    (cudaMemsetAsync, no allocation); the histogram needs no clearing.
+//  - each call clears the completion ticket and the spare words after it
+//    (cudaMemsetAsync, no allocation); the histogram needs no clearing;
+//  - errors the kernels find (an expert id outside [0, E)) are OR-ed into the
+//    array's status word, which no call clears: it accumulates until
+//    moe_assign_slots_static_status() reads and clears it, as
+//    moe_device_status() does for a workspace;
+//  - the array is placed on a device when the library's module is loaded
+//    there, which under CUDA's lazy module loading is the first call on that
+//    device; a caller that needs every later call free of that one-time
+//    placement makes one warm-up call per device first.
 #include <mutex>
 
 #include "common.cuh"
@@ -27,7 +35,7 @@
 namespace moe {
 namespace {
 
-constexpr int64_t kStaticWords = 64;              // status [0], ticket [1]; 256 B
+constexpr int64_t kStaticWords = 64;              // status [0], ticket [1], spare; 256 B
 constexpr int64_t kStaticHistInts = 1ll << 20;    // 4 MiB of histogram entries
 constexpr int kMaxDevices = 64;
 
@@ -65,20 +73,9 @@ extern "C" int moe_assign_slots_static(const moe_problem* mp, const int32_t* top
                                        int32_t* shard_routed, int32_t* shard_overflow, int32_t* row_token,
                                        int32_t* dropped, void* stream) {
     Problem p;
-    int rc = moe_capacity(mp, &p.C, &p.C_shard, &p.rows_max);  // validates the problem
+    int rc = to_problem(mp, &p);  // the same validation and derived sizes as moe_assign_slots
     if (rc != MOE_OK) return rc;
-    if (mp->flags & MOE_FLAG_REROUTE) return MOE_ERR_INVALID_ARG;  // rerouting has its own entry point
-    p.T = mp->T;
-    p.d = mp->d;
-    p.E = mp->E;
-    p.D = mp->D;
-    p.k = mp->k;
-    p.ffn = mp->ffn;
-    p.dtype = mp->dtype;
-    p.act = mp->act;
-    p.flags = mp->flags;
-    p.ffn_shared = mp->ffn_shared;
-    p.nblk = ceil_div(p.T, kAssignBlock);
+    if (p.flags & MOE_FLAG_REROUTE) return MOE_ERR_INVALID_ARG;  // rerouting has its own entry point
     if ((p.T > 0 && (!topk_idx || !slot_pos || !row_token)) || !counts_routed || !counts_kept ||
         !expert_offsets || !shard_offsets || !shard_routed || !shard_overflow)
         return MOE_ERR_INVALID_ARG;
@@ -86,9 +83,26 @@ extern "C" int moe_assign_slots_static(const moe_problem* mp, const int32_t* top
     int32_t* scratch = nullptr;
     if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
-    if (cudaMemsetAsync(scratch, 0, kStaticWords * sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the ticket and spare words; the status word [0] keeps earlier errors
+    if (cudaMemsetAsync(scratch + 1, 0, (kStaticWords - 1) * sizeof(int32_t), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     cudaError_t e = launch_assign(p, topk_idx, slot_pos, counts_routed, counts_kept, expert_offsets,
                                   shard_offsets, shard_routed, shard_overflow, row_token, dropped,
                                   scratch + kStaticWords, (int*)scratch, s);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_assign_slots_static_status(void* stream) {
+    int32_t* scratch = nullptr;
+    if (scratch_for_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    int32_t word = 0;
+    if (cudaMemcpy(&word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word != 0) {
+        const int32_t zero = 0;
+        if (cudaMemcpy(scratch, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (word & kDevTimeout) return MOE_ERR_TIMEOUT;
+    return word ? MOE_ERR_DEVICE : MOE_OK;
 }

@@ -32,6 +32,11 @@ struct Problem {
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Validates the caller's problem (MOE_OK or the status to return) and fills
+// *p with it plus the derived capacity, row bound and block count; every
+// entry point starts here (api.cu).
+int to_problem(const moe_problem* mp, Problem* p);
+
 // fp32 <-> storage type
 template <typename T>
 struct Elem;
@@ -149,6 +154,15 @@ cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, 
                                int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
                                cudaStream_t s, int32_t* fallback_idx = nullptr,
                                float* fallback_gate = nullptr, int* status = nullptr);
+
+// bf16 router on the tensor cores (route_tc.cu): top-k indices identical to
+// the fixed-order router's, gates within the tensor-core error of the
+// experts it does not recompute; no probabilities, logits or fallbacks.
+// scan.hist null: no slot-assignment count pass.  cudaErrorNotSupported when
+// the tensor-map encoder is unavailable.
+bool route_tc_eligible(const Problem& p);
+cudaError_t launch_route_tc(const Problem& p, const void* x, const void* Wg, const float* bias, int32_t* topk_idx,
+                            float* topk_gate, const AssignScan& scan, int* status, cudaStream_t s);
 
 cudaError_t launch_assign(const Problem& p, const int32_t* topk_idx, int32_t* slot_pos,
                           int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,

@@ -166,8 +166,13 @@ int moe_workspace_layout_of(const moe_problem* p, moe_workspace_layout* out);
 
 /* Router: gate computation and expert selection (notes page, formal
  * algorithm; ashishsrivastav.com phase 1).
- *   g[t,e]   = sum_i x[t,i] * Wg[e,i]  (+ bias[e])   fp32, one fused
- *              multiply-add chain over i ascending from +0, then the bias add
+ *   g[t,e]   = sum_i x[t,i] * Wg[e,i]  (+ bias[e])   fp32, in one fixed
+ *              order: the hidden index is dealt into 32 slices of runs of 8
+ *              consecutive elements (slice j holds i = 256*m + 8*j + q,
+ *              q = 0..7, m = 0, 1, ...); each slice is one fused multiply-add
+ *              chain over its i ascending from +0; the 32 slice sums are
+ *              combined by the xor butterfly o = 16, 8, 4, 2, 1 (every slice j
+ *              replaced at once by s[j] + s[j ^ o]); then the bias add
  *   probs[t] = softmax(g[t])            (temperature 1)
  *   topk_idx[t, r]  = the expert of rank r (largest logit first; equal logits
  *                     rank the lower expert first)
@@ -347,15 +352,31 @@ int moe_combine_expert_choice(const moe_problem* p, const void* yd, const float*
  *     return MOE_ERR_WORKSPACE and launch nothing;
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, once per device, that device current); make that
- *     first call before any stream capture;
- *   - all calls share the array and each starts by clearing its ticket and
- *     status words: calls whose work overlaps on the GPU (other streams, other
- *     host threads) race and must be serialised by the caller;
+ *     first call before any stream capture.  The driver places the array on a
+ *     device when it loads the library's module there, which under CUDA's
+ *     lazy module loading is that first call: a caller that needs every later
+ *     call free of that one-time placement makes one warm-up call per device;
+ *   - all calls share the array and each starts by clearing its completion
+ *     ticket: calls whose work overlaps on the GPU (other streams, other host
+ *     threads) race and must be serialised by the caller;
+ *   - an expert id outside [0, E) counts as no assignment (as in
+ *     moe_assign_slots) and sets the array's status word, which calls do not
+ *     clear; moe_assign_slots_static_status() reads and clears it;
  *   - no cudaMalloc, cudaFree or other allocating call is made. */
 int moe_assign_slots_static(const moe_problem* p, const int32_t* topk_idx, int32_t* slot_pos,
                             int32_t* counts_routed, int32_t* counts_kept, int32_t* expert_offsets,
                             int32_t* shard_offsets, int32_t* shard_routed, int32_t* shard_overflow,
                             int32_t* row_token, int32_t* dropped, void* stream);
+
+/* The device status of moe_assign_slots_static on the current device, the
+ * counterpart of moe_device_status for that workspace-free entry point (the
+ * pages have no counterpart of it either): synchronises `stream`, reads the
+ * status word of the static scratch array (errors OR-ed in by every call
+ * since the last read), clears it and returns MOE_OK, MOE_ERR_DEVICE (an
+ * expert id outside [0, E) was seen) or MOE_ERR_TIMEOUT (or MOE_ERR_CUDA if a
+ * CUDA call failed).  Allocates nothing; the word is copied to a host stack
+ * variable. */
+int moe_assign_slots_static_status(void* stream);
 
 /* Indices of the moe_routing_stats outputs. */
 enum {

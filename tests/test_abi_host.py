@@ -33,11 +33,26 @@ def _declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
-    assert len(names) == 26, names
+    assert len(names) == 27, names
     assert sorted(moe.EXPORTS) == names
     lib = moe.load()
     for n in names:
         assert hasattr(lib, n), n
+
+
+def test_route_doc_states_the_fixed_logit_order():
+    # the order the router and the oracle both use: 32 slices of runs of 8
+    # consecutive elements, one ascending fused multiply-add chain each, then
+    # the xor butterfly over offsets 16, 8, 4, 2, 1, then the bias
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    doc = src[:src.index("int moe_route(")]
+    doc = doc[doc.rindex("/*"):]
+    flat = " ".join(doc.replace("*", " ").split())
+    for phrase in ("32 slices of runs of 8 consecutive elements", "i = 256 m + 8 j + q",
+                   "q = 0..7", "ascending from +0", "xor butterfly o = 16, 8, 4, 2, 1",
+                   "s[j] + s[j ^ o]", "then the bias add"):
+        assert phrase in flat, phrase
+    assert "one fused multiply-add chain over i ascending" not in flat
 
 
 def test_status_strings():
