@@ -5,6 +5,7 @@ has no cross-GPU exchange); each rank draws its own inputs, the job time is
 the slowest rank's and the throughput counts every rank's tokens.
 """
 import os
+import time
 import socket
 
 import pytest
@@ -64,8 +65,10 @@ def test_reference_arm_prints_its_contract_line():
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    t0 = time.perf_counter()
     out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_fp32", "--steps",
-                          "1", "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=300)
+                          "2", "--warmup", "3"], cwd=root, capture_output=True, text=True, timeout=300)
+    wall_s = time.perf_counter() - t0
     assert out.returncode == 0, out.stderr[-2000:]
     line = json.loads(out.stdout.strip().splitlines()[-1])
     for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
@@ -75,3 +78,13 @@ def test_reference_arm_prints_its_contract_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["e2e"]["value"] == line["value"]
+    # the measured wall time per step: the timed steps fit in the process's run
+    assert 0 < line["steps"] * line["ms_per_step"] * 1e-3 < wall_s
+    assert line["extrapolated_ms_per_layer"] > 0
+    # the same config object as the GPU arm prints for this workload
+    import bench
+    wl = bench.moe_inputs.WORKLOADS["tiny_fp32"]
+    import oracle
+    C = oracle.capacity(wl.T, wl.k, wl.E, wl.D, wl.capacity_factor)[0]
+    assert line["config"] == bench.workload_config(wl, C, line["config"]["kept"], line["config"]["dropped"], 1)
+    assert line["config"]["kept"] + line["config"]["dropped"] == wl.T * wl.k
