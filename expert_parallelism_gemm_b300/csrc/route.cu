@@ -506,6 +506,9 @@ cudaError_t launch_route(const Problem& p, const void* x, const void* Wg, const 
                          int32_t* fallback_idx, float* fallback_gate, int* status) {
     if (p.T == 0) return cudaSuccess;
     AssignScan none{};
+    // the tensor-core router when only indices and gates are asked for
+    if (route_tc_eligible(p) && !probs && !logits && !fallback_idx)
+        return launch_route_tc(p, x, Wg, bias, topk_idx, topk_gate, none, status, s);
     if (p.dtype == MOE_BF16)
         return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits, fallback_idx,
                                              fallback_gate, status, none, s);
@@ -517,6 +520,8 @@ cudaError_t launch_route_count(const Problem& p, const void* x, const void* Wg, 
                                int32_t* topk_idx, float* topk_gate, const AssignScan& scan,
                                cudaStream_t s, int32_t* fallback_idx, float* fallback_gate, int* status) {
     if (p.T == 0) return cudaErrorInvalidValue;  // callers handle T = 0 without a launch
+    if (route_tc_eligible(p) && !fallback_idx)
+        return launch_route_tc(p, x, Wg, bias, topk_idx, topk_gate, scan, status, s);
     if (p.dtype == MOE_BF16)
         return launch_route_t<__nv_bfloat16>(p, x, Wg, bias, topk_idx, topk_gate, nullptr, nullptr, fallback_idx,
                                              fallback_gate, status, scan, s);

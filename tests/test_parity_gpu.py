@@ -100,9 +100,15 @@ def test_route(case):
     np.testing.assert_array_equal(idx.cpu().numpy(), o["idx"])
     assert_probs(gate.cpu().numpy(), o["gate"], "gate")
     assert_probs(probs.cpu().numpy(), o["probs"], "probs")
-    # without the optional probability output the decisions are the same
+    # without the optional probability output the bf16 router runs on the
+    # tensor cores: the same indices bit for bit, gates within the tolerance
     idx2, gate2, _ = dev.route(want_probs=False)
-    assert torch.equal(idx2, idx) and torch.equal(gate2, gate)
+    np.testing.assert_array_equal(idx2.cpu().numpy(), o["idx"])
+    assert_probs(gate2.cpu().numpy(), o["gate"], "gate without probs")
+    if wl.dtype == "f32":  # the fp32 router has one path
+        assert torch.equal(gate2, gate)
+    idx3, gate3, _ = dev.route(want_probs=False)
+    assert torch.equal(idx3, idx2) and torch.equal(gate3, gate2)  # deterministic
     assert dev.status() == moe.MOE_OK
 
 
