@@ -90,8 +90,10 @@ constexpr int kGramXCol = 0;
 constexpr int kGramWCol = 128;
 constexpr int kLogitCol0 = 256;
 constexpr int kMaxGroups = 16;
+constexpr int kLogitPitch = kTM + 1;  // floats per expert row of the epilogue's logit table
+constexpr int kEPerLane = 4;          // experts per lane when a warp walks one token (E <= 128)
 constexpr int kMaxStages = 10;
-constexpr int kStageBudget = 192 * 1024;      // shared memory for the stage ring
+constexpr int kStageBudget = 200 * 1024;      // shared memory for the stage ring and the logit table
 constexpr uint64_t kTcTimeoutNs = 2000000000ull;  // 2 s: far above any legitimate wait
 // tensor-core accumulation model: error per MMA step <= kHwUlp * magnitude
 constexpr double kHwUlp = 1.0 / (1 << 18);
@@ -282,6 +284,16 @@ __device__ __forceinline__ void fixed_order_logits(const __nv_bfloat16* xr, cons
     }
 }
 
+// Order-preserving 32-bit image of a float (larger value, larger unsigned
+// bits; -0 must have been turned into +0 first) and its inverse.
+__device__ __forceinline__ uint32_t order_bits(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float from_order_bits(uint32_t o) {
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
 // (v, e) ranks before entry p of a list sorted by value descending, index
 // ascending on ties (an entry with index -1 is empty).
 __device__ __forceinline__ bool ranks_before(float v, int e, float lvp, int lep) {
@@ -317,13 +329,11 @@ __device__ __forceinline__ void list_insert(float (&lv)[L], int (&le)[L], int n,
 }
 
 
-// KM: largest k this instance serves; EWM: 32-expert words of the candidate
-// mask and of the per-token logit registers (E <= 32 * EWM <= 128)
-template <int KM, int EWM>
+// KM: largest k this instance serves
+template <int KM>
 __global__ void __launch_bounds__(kRtThreads, 1)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, const RtArgs a,
                 const AssignScan scan) {
-    constexpr int NPM = 32 * EWM;  // logit registers per token
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = s_u32(smem_raw);
     uint8_t* ring = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -443,38 +453,44 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
         asm volatile("bar.sync 1, 128;" ::: "memory");
         const float* bias = sh.bias;  // zero without a router bias
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
+        // logit table [n_pad][kLogitPitch]: expert-major, one column per token of
+        // the tile (the pitch keeps both a thread's row walk and a warp's
+        // expert walk free of bank conflicts)
+        float* gt = reinterpret_cast<float*>(ring + (size_t)S * stage_bytes + sizeof(RtShared));
+        const int row = q * 32 + lane;  // this thread's token within the tile
         float wmax = 0.0f;
         uint32_t tphase = 0;
         bool first = true;
         for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            const int row = q * 32 + lane;               // this thread's token within the tile
             const int64_t t = (int64_t)tile * kTM + row;
             const bool valid = t < a.T;
             const int64_t blk = ((int64_t)tile * kTM + q * 32) / kAssignBlock;  // assignment block of this warp
 
-            // the groups' partial logits, added in ascending group order as each
-            // group's MMAs complete (while later groups still stream in)
-            float gh[NPM];
-#pragma unroll
-            for (int i = 0; i < NPM; ++i) gh[i] = 0.0f;
+            // the groups' partial logits, added into the table in ascending
+            // group order as each group's MMAs complete (while later groups
+            // still stream in)
             bool ok = true;
             for (int j = 0; j < nc && ok; ++j) {
                 ok = __all_sync(0xffffffffu, bar_wait(s_u32(&sh.gfull[j]), tphase, abort_flag, status));
                 if (!ok) break;
                 tc_after();
                 const uint32_t tg = tmem_base + lanes + (uint32_t)(kLogitCol0 + j * NP);
+                for (int c0 = 0; c0 < NP; c0 += 32) {
+                    float v0[16], v1[16];
+                    tmem_ld16_nowait(tg + c0, v0);
+                    if (c0 + 16 < NP) tmem_ld16_nowait(tg + c0 + 16, v1);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int c0 = 0; c0 < NPM; c0 += 32) {
-                    if (c0 < NP) {
-                        float v0[16], v1[16];
-                        tmem_ld16_nowait(tg + c0, v0);
-                        if (c0 + 16 < NP) tmem_ld16_nowait(tg + c0 + 16, v1);
-                        tmem_wait_ld();
+                    for (int i = 0; i < 16; ++i) {
+                        float* p0 = gt + (c0 + i) * kLogitPitch + row;
+                        *p0 = j ? *p0 + v0[i] : v0[i];
+                    }
+                    if (c0 + 16 < NP) {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) gh[c0 + i] += v0[i];
-                        if (c0 + 16 < NP)
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) gh[c0 + 16 + i] += v1[i];
+                        for (int i = 0; i < 16; ++i) {
+                            float* p1 = gt + (c0 + 16 + i) * kLogitPitch + row;
+                            *p1 = j ? *p1 + v1[i] : v1[i];
+                        }
                     }
                 }
             }
@@ -502,18 +518,18 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                     }
                 }
             }
-            // every value needed is in registers: the accumulators are free for
-            // the next tile
+            // everything needed is in registers and shared memory: the
+            // accumulators are free for the next tile
             tc_before();
             __syncwarp();
             if (lane == 0) bar_arrive(s_u32(&sh.tempty));
             if (first) {
-                // max_e ||Wg_e||^2 (rows past E hold x rows: excluded)
+                // max_e ||Wg_e||^2 (rows past E hold x rows: excluded); the four
+                // warps' maxima meet on an mbarrier (a bounded wait, so a warp
+                // that gave up earlier cannot leave the others stuck)
                 float wm = row < E ? fmaxf(wsq, 0.0f) : 0.0f;
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-                // the four warps' maxima meet on an mbarrier (a bounded wait,
-                // so a warp that gave up earlier cannot leave the others stuck)
                 if (lane == 0) {
                     atomicMax(reinterpret_cast<int*>(&sh.wmax_sq), __float_as_int(wm));
                     bar_arrive(s_u32(&sh.wdone));
@@ -523,8 +539,12 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 first = false;
             }
 
-            // pass A: bias; the k+1 largest g^ + b (ties to the lower expert);
-            // max |g^ + b|
+            // the warp's 32 tokens, four at a time, lane = expert (expert
+            // lane + 32 i): per token the k+1 largest g^ + b by repeated argmax
+            // (a warp max of order-preserving bits, then the lowest expert
+            // holding it), max |g^ + b|, and the softmax denominator over every
+            // expert (an xor-butterfly sum of exp(g^ + b - m), m = the largest);
+            // the token's own lane keeps the results
             const int K1 = k < E ? k + 1 : k;
             float lv[KM + 1];
             int le[KM + 1];
@@ -533,15 +553,70 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 lv[i] = -CUDART_INF_F;
                 le[i] = -1;
             }
-            float maxabs = 0.0f;
+            float maxabs = 0.0f, s_all = 0.0f;
+            for (int j0 = 0; j0 < 32; j0 += 4) {
+                float v[4][kEPerLane];
 #pragma unroll
-            for (int e = 0; e < NPM; ++e) {
-                if (e < E) {
-                    gh[e] += bias[e];
-                    maxabs = fmaxf(maxabs, fabsf(gh[e]));
-                    list_insert(lv, le, K1, gh[e], e);
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int i = 0; i < kEPerLane; ++i) {
+                        const int e = lane + 32 * i;
+                        // + 0.0f turns -0 into +0, so order-preserving bits tie as the values do
+                        v[u][i] = e < E ? gt[e * kLogitPitch + q * 32 + j0 + u] + bias[e] + 0.0f : -CUDART_INF_F;
+                    }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float la = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kEPerLane; ++i)
+                        if (lane + 32 * i < E) la = fmaxf(la, fabsf(v[u][i]));
+                    la = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(la)));
+                    float top = 0.0f;
+#pragma unroll
+                    for (int r = 0; r <= KM; ++r) {
+                        if (r < K1) {
+                            // this lane's largest remaining value (lower expert first)
+                            float bv = -CUDART_INF_F;
+                            int bi = 0;
+#pragma unroll
+                            for (int i = 0; i < kEPerLane; ++i)
+                                if (v[u][i] > bv) {
+                                    bv = v[u][i];
+                                    bi = i;
+                                }
+                            const uint32_t ob = order_bits(bv);
+                            const uint32_t om = __reduce_max_sync(0xffffffffu, ob);
+                            const int be = (int)__reduce_min_sync(0xffffffffu,
+                                                                  ob == om ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+                            const float val = from_order_bits(om);
+                            if ((be & 31) == lane) {
+#pragma unroll
+                                for (int i = 0; i < kEPerLane; ++i)
+                                    if (i == (be >> 5)) v[u][i] = -CUDART_INF_F;
+                            }
+                            if (r == 0) top = val;
+                            if (lane == j0 + u) {
+                                lv[r] = val;
+                                le[r] = be;
+                            }
+                        }
+                    }
+                    // the removed entries are restored from the table for the sum
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kEPerLane; ++i) {
+                        const int e = lane + 32 * i;
+                        if (e < E) sum += __expf(gt[e * kLogitPitch + q * 32 + j0 + u] + bias[e] - top);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                    if (lane == j0 + u) {
+                        maxabs = la;
+                        s_all = sum;
+                    }
                 }
             }
+            const float m = lv[0];  // the largest g^ + b: the softmax shift
             const float xn = sqrtf(fmaxf(xsq, 0.0f) * a.gram_scale) * (1.0f + 1e-6f);
             const float theta2 = 2.0f * (a.c_d * xn * wmax + 2.4e-7f * maxabs);
             // certain: the k+1 largest g^ are more than 2 theta apart; vk = the k-th
@@ -552,33 +627,16 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 if (r + 1 < K1) certain = certain && (lv[r] - lv[r + 1] > theta2);
                 if (r == k - 1) vk = lv[r];
             }
-            const float m = lv[0];  // softmax shift
             const bool redo = valid && !certain;
-
-            // pass B: the candidate set U of an uncertain token, every expert
-            // within 2 theta of the k-th; pass C: the softmax denominator over
-            // the experts outside U, ascending
-            uint32_t mask[EWM];
-            float s_rest = 0.0f;
-#pragma unroll
-            for (int w = 0; w < EWM; ++w) {
-                uint32_t bits = 0u;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int e = 32 * w + i;
-                    if (e < E && redo && gh[e] >= vk - theta2) bits |= 1u << i;
-                }
-                mask[w] = bits;
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int e = 32 * w + i;
-                    if (e < E && !((bits >> i) & 1u)) s_rest += expf(gh[e] - m);
-                }
-            }
+            // an uncertain token's candidates U: every expert within 2 theta of
+            // its k-th largest
+            const float band = vk - theta2;
 
             // a certain token keeps its k largest g^; an uncertain one ranks
             // the fixed-order logits of U, recomputed one token at a time
-            // across the warp, and adds their exp(g - m) to the denominator
+            // across the warp (its candidates found by a ballot over the
+            // table), and swaps their terms of the denominator for
+            // exp(g - m) of the recomputed values
             float rv[KM];
             int re[KM];
 #pragma unroll
@@ -590,17 +648,19 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
             const uint32_t redo_warp = __ballot_sync(0xffffffffu, redo);
             for (uint32_t todo = redo_warp; todo; todo &= todo - 1) {
                 const int j = __ffs(todo) - 1;
+                const float band_j = __shfl_sync(0xffffffffu, band, j);
                 const __nv_bfloat16* xr = a.x + (size_t)((int64_t)tile * kTM + q * 32 + j) * d;
-#pragma unroll
-                for (int w = 0; w < EWM; ++w) {
-                    uint32_t bits = __shfl_sync(0xffffffffu, mask[w], j);
+                for (int c0 = 0; c0 < E; c0 += 32) {
+                    const int ec = c0 + lane;
+                    const float gc = ec < E ? gt[ec * kLogitPitch + q * 32 + j] + bias[ec] : -CUDART_INF_F;
+                    uint32_t bits = __ballot_sync(0xffffffffu, gc >= band_j);
                     while (bits) {
                         int e2[2] = {0, 0};
                         int nb = 0;
 #pragma unroll
                         for (int z = 0; z < 2; ++z)
                             if (bits) {
-                                e2[z] = 32 * w + __ffs(bits) - 1;
+                                e2[z] = c0 + __ffs(bits) - 1;
                                 bits &= bits - 1;
                                 nb = z + 1;
                             }
@@ -612,7 +672,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                                 if (z < nb) {
                                     const float g = g2[z] + bias[e2[z]];
                                     list_insert(rv, re, k, g, e2[z]);
-                                    s_exact += expf(g - m);
+                                    const float gh = gt[e2[z] * kLogitPitch + row] + bias[e2[z]];
+                                    s_exact += __expf(g - m) - __expf(gh - m);
                                 }
                         }
                     }
@@ -620,7 +681,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
             }
 
             if (valid) {
-                const float inv = 1.0f / (s_rest + s_exact);
+                const float inv = 1.0f / (s_all + s_exact);
                 float den = 0.0f;
 #pragma unroll
                 for (int r = 0; r < KM; ++r)
@@ -646,6 +707,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                             scan.hist[((size_t)key * k + r) * scan.nblk + blk] = __popc(same);
                     }
             }
+            // the table is rewritten by the next tile only after every warp of
+            // this one is done with it (each warp owns its own token columns)
+            __syncwarp();
             tphase ^= 1u;
         }
     }
@@ -699,7 +763,12 @@ int sm_count() {
 
 }  // namespace
 
-bool route_tc_eligible(const Problem& p) { return p.dtype == MOE_BF16 && p.T > 0 && p.E <= 128; }
+// Up to 16 experts the fixed-order SIMT router is faster (its E multiply-adds
+// per loaded element cost less than this kernel's Gram products and per-tile
+// epilogue; measured at 8 experts: 17 against 28 us at T = 4096, 140 against
+// 162 us at T = 32768, d = 4096); above 128 the per-token logit table no
+// longer fits next to the stage ring.
+bool route_tc_eligible(const Problem& p) { return p.dtype == MOE_BF16 && p.T > 0 && p.E > 16 && p.E <= 128; }
 
 cudaError_t launch_route_tc(const Problem& p, const void* x, const void* Wg, const float* bias, int32_t* topk_idx,
                             float* topk_gate, const AssignScan& scan, int* status, cudaStream_t s) {
@@ -712,7 +781,10 @@ cudaError_t launch_route_tc(const Problem& p, const void* x, const void* Wg, con
     a.k = p.k;
     a.n_pad = (p.E + 15) / 16 * 16;
     const int stage_bytes = (a.n_pad + kTM) * 128;
-    a.stages = std::min(kMaxStages, kStageBudget / stage_bytes);
+    // the table holds n_pad rows: the group sums write every accumulator
+    // column, the padding ones included (never read back)
+    const int table_bytes = a.n_pad * kLogitPitch * (int)sizeof(float);
+    a.stages = std::min(kMaxStages, (kStageBudget - table_bytes) / stage_bytes);
     a.renorm = (p.flags & MOE_FLAG_RENORM) != 0;
     // accumulation groups: as many as the columns after the Gram block hold
     const int nstages = (int)ceil_div(p.d, kBK);
@@ -740,7 +812,7 @@ cudaError_t launch_route_tc(const Problem& p, const void* x, const void* Wg, con
     if (!map_sw128(enc, &mx, x, (uint64_t)p.T, (uint64_t)p.d, kTM) ||
         !map_sw128(enc, &mw, Wg, (uint64_t)p.E, (uint64_t)p.d, (uint32_t)a.n_pad))
         return cudaErrorInvalidValue;
-    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + sizeof(RtShared);
+    const size_t smem = 1024 + (size_t)a.stages * stage_bytes + sizeof(RtShared) + (size_t)table_bytes;
     const int ntiles = (int)ceil_div(p.T, kTM);
     const unsigned grid = (unsigned)std::min(ntiles, sm_count());
     auto run = [&](auto kern) {
@@ -748,16 +820,9 @@ cudaError_t launch_route_tc(const Problem& p, const void* x, const void* Wg, con
         if (e != cudaSuccess) return e;
         return launch_k(kern, dim3(grid), dim3(kRtThreads), smem, s, mx, mw, a, scan);
     };
-    // instances: k <= 2 or <= 8; 32, 64 or 128 logit registers per token
-    const int ew = (p.E + 31) / 32;
-    if (p.k <= 2) {
-        if (ew == 1) return run(route_tc_kernel<2, 1>);
-        if (ew == 2) return run(route_tc_kernel<2, 2>);
-        return run(route_tc_kernel<2, 4>);
-    }
-    if (ew == 1) return run(route_tc_kernel<8, 1>);
-    if (ew == 2) return run(route_tc_kernel<8, 2>);
-    return run(route_tc_kernel<8, 4>);
+    // instances: k <= 2 or <= 8
+    if (p.k <= 2) return run(route_tc_kernel<2>);
+    return run(route_tc_kernel<8>);
 }
 
 }  // namespace moe

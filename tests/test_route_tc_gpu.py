@@ -11,8 +11,10 @@ input; gates must be within 1e-5 relative.  The cases below make that
 recompute path do the work: experts with identical or nearly identical router
 rows (exact and near ties in every token), rows that are scaled copies of
 each other, heavy-tailed activations, a bias that forces ties, and shapes
-across the kernel's instances (k <= 2 or <= 8; 8 to 256 experts; ragged
-tiles).  Each case prints the share of tokens whose fixed-order top-(k+1)
+across the kernel's instances (k <= 2 or <= 8; 24 to 128 experts, padded
+and unpadded; ragged tiles; one token).  The tensor-core path serves 17 to
+128 experts; the 256-expert case checks the fixed-order router that takes
+over above that range.  Each case prints the share of tokens whose fixed-order top-(k+1)
 gaps lie inside twice the bound, i.e. roughly the share of tokens the kernel
 had to re-rank.
 """
@@ -41,7 +43,7 @@ def _bf16_ulp_up(t):
 def _case(name):
     g = torch.Generator().manual_seed(zlib.crc32(name.encode()))
     if name == "duplicate_rows":
-        wl = Workload(name, T=1000, d=256, E=8, D=4, k=2, ffn=64, capacity_factor=1.0, seed=60)
+        wl = Workload(name, T=1000, d=256, E=24, D=4, k=2, ffn=64, capacity_factor=1.0, seed=60)
         inp = moe_inputs.make_inputs(wl)
         inp.Wg[5] = inp.Wg[3]
         inp.Wg[6] = inp.Wg[0]
@@ -55,7 +57,7 @@ def _case(name):
     elif name == "scaled_copies":
         # every odd expert is its even neighbour scaled by 1 + 2^-7: exact
         # logits differ by under 1% and the order flips with the sign
-        wl = Workload(name, T=2048, d=1024, E=16, D=4, k=4, ffn=64, capacity_factor=1.0, seed=62)
+        wl = Workload(name, T=2048, d=1024, E=32, D=4, k=4, ffn=64, capacity_factor=1.0, seed=62)
         inp = moe_inputs.make_inputs(wl)
         for e in range(1, wl.E, 2):
             inp.Wg[e] = (inp.Wg[e - 1].float() * (1 + 2.0**-7)).to(torch.bfloat16)
@@ -76,10 +78,10 @@ def _case(name):
         inp = moe_inputs.make_inputs(wl)
         inp.Wg[200:] = inp.Wg[100:156]
     elif name == "one_token":
-        wl = Workload(name, T=1, d=64, E=8, D=4, k=2, ffn=64, capacity_factor=1.0, seed=66)
+        wl = Workload(name, T=1, d=64, E=24, D=4, k=2, ffn=64, capacity_factor=1.0, seed=66)
         inp = moe_inputs.make_inputs(wl)
     elif name == "ragged_129":
-        wl = Workload(name, T=129, d=4096, E=8, D=8, k=2, ffn=64, capacity_factor=math.inf, seed=67)
+        wl = Workload(name, T=129, d=4096, E=40, D=8, k=2, ffn=64, capacity_factor=math.inf, seed=67)
         inp = moe_inputs.make_inputs(wl)
         inp.Wg[7] = inp.Wg[2]
     else:
