@@ -433,6 +433,10 @@ def run_ours(args, rank, world, local_rank):
         dispatch_bytes = disp_tokens * wl.d * eb + kept * wl.d * eb
         combine_bytes = kept * wl.d * eb + wl.T * wl.d * eb + wl.T * wl.k * 12
         weight_bytes = mats * wl.d * wl.ffn * eb * n_exp_used
+        # the expert FFN's DRAM floor: each used expert's weights once, plus xd
+        # read, h written and read back, yd written, per kept row
+        ffn_bytes = weight_bytes + kept * (2 * wl.d + 2 * wl.ffn) * eb
+        hbm_bound = ffn_bytes / (hbm_gbs * 1e9) > ffn_flops / (bf16_tf * 1e12)
         gb = lambda b, ms: b / (ms * 1e-3) / 1e9
         kernels = {
             "route": {"ms": per_call["route"], "GB_s": gb(route_bytes, per_call["route"]),
@@ -442,7 +446,9 @@ def run_ours(args, rank, world, local_rank):
                          "frac_hbm": gb(dispatch_bytes, per_call["dispatch"]) / hbm_gbs},
             "expert_ffn": {"ms": per_call["expert_ffn"], "TFLOP_s": achieved_tf,
                            "frac_bf16": achieved_tf / bf16_tf,
-                           "weight_GB_s": gb(weight_bytes, per_call["expert_ffn"])},
+                           "weight_GB_s": gb(weight_bytes, per_call["expert_ffn"]),
+                           "GB_s": gb(ffn_bytes, per_call["expert_ffn"]),
+                           "frac_hbm": gb(ffn_bytes, per_call["expert_ffn"]) / hbm_gbs},
             "combine": {"ms": per_call["combine"], "GB_s": gb(combine_bytes, per_call["combine"]),
                         "frac_hbm": gb(combine_bytes, per_call["combine"]) / hbm_gbs},
             "shared_expert_ffn": None if shared_ms is None else {
@@ -474,14 +480,12 @@ def run_ours(args, rank, world, local_rank):
             "dtype": wl.dtype,
             "data": "synthetic (seeded torch generator on the device; random-init weights)",
             "config": workload_config(wl, C, kept, n_dropped, world),
-            "roofline": {"kernel": "moe_expert_ffn (one 2-SM tcgen05 launch: gate/up + down)", "bound": "tensor",
-                         "achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
-                         "frac": achieved_tf / bf16_tf,
-                         "traffic": FFN_DRAM_BYTES.get(wl.name),
-                         "peak_source": (f"{peak_src} bf16 sustained (a {per_call['expert_ffn']:.1f} ms launch "
-                                         f"runs under the power limit)" if sustained else f"{peak_src} bf16 burst"),
-                         "frac_burst": achieved_tf / bf16_burst, "frac_sustained": achieved_tf / bf16_sust,
-                         "algorithmic": f"2*3*d*ffn flops per kept row x {kept} rows"},
+            "roofline": ffn_roofline(hbm_bound, achieved_tf, bf16_tf, bf16_burst, bf16_sust,
+                                     gb(ffn_bytes, per_call["expert_ffn"]), hbm_gbs, ffn_bytes, kept,
+                                     FFN_DRAM_BYTES.get(wl.name),
+                                     (f"{peak_src} bf16 sustained (a {per_call['expert_ffn']:.1f} ms launch "
+                                      f"runs under the power limit)" if sustained else f"{peak_src} bf16 burst"),
+                                     peak_src, mats),
             "kernels": kernels,
             "e2e": {"value": job_tokens_per_s(wl.T, world, args.steps, e2e_ms_max), "unit": "tokens/s",
                     "h2d_bytes_per_step": wl.T * wl.d * eb, "d2h_bytes_per_step": wl.T * wl.d * eb,
@@ -495,6 +499,25 @@ def run_ours(args, rank, world, local_rank):
             "clocks": clocks,
         }
     return out
+
+
+def ffn_roofline(hbm_bound, achieved_tf, bf16_tf, bf16_burst, bf16_sust, achieved_gbs, hbm_gbs, ffn_bytes,
+                 kept, traffic, tensor_src, peak_src, mats):
+    """The expert FFN launch against whichever floor is higher for this shape:
+    the tensor pipe (flops / bf16 peak) or HBM (its algorithmic bytes / copy
+    bandwidth).  Experts with few rows each stream their weights faster than
+    the MMAs on them can finish, and are HBM-bound."""
+    kernel = "moe_expert_ffn (one persistent tcgen05 launch: gate/up + down)"
+    both = {"frac_burst": achieved_tf / bf16_burst, "frac_sustained": achieved_tf / bf16_sust,
+            "tflops": achieved_tf, "gbs": achieved_gbs, "frac_hbm": achieved_gbs / hbm_gbs}
+    if hbm_bound:
+        return {"kernel": kernel, "bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                "frac": achieved_gbs / hbm_gbs, "traffic": traffic, "peak_source": f"{peak_src} HBM copy",
+                **both, "algorithmic": f"{mats}*d*ffn*b per used expert + (2*d + 2*ffn)*b per kept row "
+                                       f"({ffn_bytes} B, {kept} rows)"}
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved_tf, "peak": bf16_tf, "unit": "TFLOP/s",
+            "frac": achieved_tf / bf16_tf, "traffic": traffic, "peak_source": tensor_src,
+            **both, "algorithmic": f"2*{mats}*d*ffn flops per kept row x {kept} rows"}
 
 
 def launches_per_step(wl) -> int:

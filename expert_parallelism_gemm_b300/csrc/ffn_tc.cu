@@ -35,6 +35,13 @@
 // stride = number of clusters.  An m-tile with no rows (odd count) still takes
 // part in its pair's loads and MMAs and stores nothing.
 //
+// When the capacity keeps every expert within one 128-row tile (C <= 128, as
+// in layers of many small experts), a pair tile would be at least half
+// padding; the kernel then runs in its one-CTA form instead: no clusters,
+// 128 x 256 tiles with the one-SM MMA (tcgen05.mma.cta_group::1, M = 128),
+// each CTA loading its A tile and the whole 256-row weight tile (4 stages of
+// 48 KB), release counters per (expert, m-tile).  Everything else is shared.
+//
 // Per CTA (one per SM, 192 threads):
 //   warp 0   TMA producer: its A tile [128 x 64] and its B half [128 x 64]
 //            per stage (128-byte swizzle, 6 stages of 32 KB); both CTAs'
@@ -64,20 +71,29 @@ constexpr int BM = 128;       // rows per tile (MMA M)
 constexpr int BN = 256;       // MMA N (gate/up: 128 + 128 columns)
 constexpr int BK = 64;        // K per stage (one 128-byte swizzle atom of bf16)
 constexpr int UK = 16;        // K per MMA instruction
-constexpr int STAGES = 6;
+constexpr int kMaxStages = 6;
 constexpr int kTcThreads = 192;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES / 2;  // own A tile + own half of B
 constexpr int TMEM_COLS = 512;
 constexpr int kMaxE = 256;
-constexpr int kCluster = 2;   // CTAs per cluster (the pair of one 2-SM MMA)
+// The kernel runs in one of two forms, CL = CTAs per cluster:
+//  CL = 2: pairs of CTAs compute 256-row tiles with the 2-SM MMA; each CTA
+//          loads its 128 A rows and half of the 256-row weight tile;
+//  CL = 1: single CTAs compute 128-row tiles (M = 128) and load the whole
+//          weight tile; used when the capacity keeps every expert within one
+//          128-row tile, where a pair tile would be at least half padding.
+// stage = own A tile + own share of the weight tile
+template <int CL>
+__host__ __device__ constexpr int stage_bytes() { return A_BYTES + B_BYTES / CL; }
+template <int CL>
+__host__ __device__ constexpr int num_stages() { return CL == 2 ? 6 : 4; }
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s: far above any legitimate wait
 
 // shared-memory map after the 1024-aligned stage area
 struct __align__(8) TcShared {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -97,23 +113,27 @@ struct __align__(8) TcShared {
 constexpr int kStgCols = 64;
 constexpr int kStgPitch = kStgCols * 2 + 16;  // bytes; rows 16 B apart in bank space
 constexpr int kStgWarpBytes = 32 * kStgPitch;
-constexpr size_t kStgOffset = (size_t)STAGES * STAGE_BYTES + ((sizeof(TcShared) + 127) / 128) * 128;
-constexpr size_t kSmemBytes = 1024 + kStgOffset + 4 * kStgWarpBytes;
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+template <int CL>
+__host__ __device__ constexpr size_t stg_offset() {
+    return (size_t)num_stages<CL>() * stage_bytes<CL>() + ((sizeof(TcShared) + 127) / 128) * 128;
+}
+template <int CL>
+__host__ __device__ constexpr size_t smem_bytes() { return 1024 + stg_offset<CL>() + 4 * kStgWarpBytes; }
+static_assert(smem_bytes<2>() <= 227 * 1024 && smem_bytes<1>() <= 227 * 1024, "shared memory");
 
 struct FfnArgs {
     int E, d, ffn, rows_max;
     int n1, k1;    // gate/up: n-tiles of 128 output columns per expert, k-blocks over d
     int n2, k2;    // down: n-tiles of 256 output columns per expert, k-blocks over ffn
-    int mp_cap;    // bound on m-tile pairs per expert
+    int mp_cap;    // bound on tile units (m-tile pairs, or m-tiles when CL = 1) per expert
     int lag;       // tiles placed between an expert's last gate/up tile and its down tiles
     const int32_t* expert_offsets;  // null: one expert whose rows are 0..rows_max-1
     __nv_bfloat16* h;
     __nv_bfloat16* yd;
     int* status;
     // [0] exit ticket; [1 + e * mp_cap + mp] epilogue-warp releases of the
-    // gate/up pair tiles of (expert e, m-pair mp).  Zero at launch; the last
-    // CTA to leave zeroes it again.
+    // gate/up tiles of (expert e, unit mp).  Zero at launch; the last CTA to
+    // leave zeroes it again.
     int* sync;
 };
 
@@ -181,6 +201,13 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
         : "memory");
 }
+// A tile into this CTA's shared memory, completing on this CTA's barrier.
+__device__ __forceinline__ void tma_load_2d_own(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
 // shared::cluster address of the same shared variable in CTA `rank`
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
     uint32_t r;
@@ -229,6 +256,22 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a, uint6
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// One-SM MMA (M = 128): A, B and D all in this CTA.
+__device__ __forceinline__ void mma_bf16_one(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_one(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 // Arrive on the barrier at offset `bar` of this CTA once the MMAs issued so
 // far complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -259,11 +302,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&b);
 }
 
-// Tile -> (kind, expert, m-tile of this CTA, n-tile, m-pair).  Segment s
-// covers the tiles [seg_start[s], seg_start[s+1]) of one kind and expert, in
-// (n-tile, m-pair) order with the m-pair fastest, so consecutive tiles share
-// the weight tile.  An expert with mte m-tiles has ceil(mte / 2) m-tile
-// pairs; rank r of the cluster takes m-tile 2 * pair + r.
+// Tile units of an expert with `rows` rows: m-tile pairs (CL = 2) or m-tiles.
+template <int CL>
+__host__ __device__ __forceinline__ int tile_units(int rows) {
+    const int mte = (rows + BM - 1) / BM;
+    return CL == 2 ? (mte + 1) / 2 : mte;
+}
+
+// Tile -> (kind, expert, m-tile of this CTA, n-tile, unit).  Segment s covers
+// the tiles [seg_start[s], seg_start[s+1]) of one kind and expert, in
+// (n-tile, unit) order with the unit fastest, so consecutive tiles share the
+// weight tile.  A unit is an m-tile pair (CL = 2: rank r of the cluster takes
+// m-tile 2 * pair + r) or one m-tile (CL = 1).
+template <int CL>
 __device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int n1, int n2, int rank, int& kind,
                                             int& e, int& mt, int& nt, int& mp) {
     int lo = 0, hi = S.nseg - 1;
@@ -275,12 +326,12 @@ __device__ __forceinline__ void tile_coords(int tile, const TcShared& S, int n1,
     kind = S.seg_info[lo] >> 16;
     e = S.seg_info[lo] & 0xffff;
     const int local = tile - S.seg_start[lo];
-    const int mpe = ((S.offs[e + 1] - S.offs[e] + BM - 1) / BM + 1) / 2;
+    const int mpe = tile_units<CL>(S.offs[e + 1] - S.offs[e]);
     (void)n1;
     (void)n2;
     nt = local / mpe;
     mp = local - nt * mpe;
-    mt = 2 * mp + rank;
+    mt = CL * mp + rank;
 }
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -289,6 +340,7 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
     return v;
 }
 
+template <int CL>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
               const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmA2,
@@ -296,12 +348,14 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t* stages = smem_raw + ((1024 - (raw & 1023)) & 1023);
+    constexpr int STAGES = num_stages<CL>();
+    constexpr int STAGE_BYTES = stage_bytes<CL>();
     TcShared& S = *reinterpret_cast<TcShared*>(stages + (size_t)STAGES * STAGE_BYTES);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = args.E;
-    const int rank = (int)cluster_rank();
-    const int cluster = blockIdx.x / kCluster, nclusters = gridDim.x / kCluster;
-    constexpr uint16_t kPairMask = (1u << kCluster) - 1;
+    const int rank = CL == 2 ? (int)cluster_rank() : 0;
+    const int cluster = blockIdx.x / CL, nclusters = gridDim.x / CL;
+    constexpr uint16_t kPairMask = (1u << CL) - 1;
     const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
@@ -311,19 +365,27 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&S.tfull[b]), 1);
-            mbar_init(smem_u32(&S.tempty[b]), 4 * kCluster);  // leader: epilogue warps of both CTAs
+            mbar_init(smem_u32(&S.tempty[b]), 4 * CL);  // leader: epilogue warps of every CTA of the cluster
         }
         mbar_init(smem_u32(&S.drain), 1);
         S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        // one warp of each CTA of the pair allocates together
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&S.tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        if constexpr (CL == 2) {
+            // one warp of each CTA of the pair allocates together
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&S.tmem_base)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(&S.tmem_base)),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     // global memory only from here on (earlier kernels on the stream are done)
     dep_wait();
@@ -346,7 +408,7 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
             // segment follows once `lag` further tiles have been placed after
             // its gate/up segment (or at the end)
             int pos = 0, nseg = 0, qh = 0, qt = 0;
-            auto pairs = [&](int e) { return ((S.offs[e + 1] - S.offs[e] + BM - 1) / BM + 1) / 2; };
+            auto pairs = [&](int e) { return tile_units<CL>(S.offs[e + 1] - S.offs[e]); };
             auto place_down = [&](int e) {
                 S.seg_start[nseg] = pos;
                 S.seg_info[nseg++] = (1 << 16) | e;
@@ -371,7 +433,7 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
     tc_fence_before();
     __syncthreads();
     // both CTAs' barriers are initialised before either signals the other
-    cluster_sync();
+    if constexpr (CL == 2) cluster_sync();
     tc_fence_after();
 
     const int total_tiles = S.total_tiles;
@@ -388,27 +450,36 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
         for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
         for (int tile = cluster; tile < total_tiles && !*abort_flag; tile += nclusters) {
             int kind, e, mt, nt, mp;
-            tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
+            tile_coords<CL>(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
             const int a_row = S.offs[e] + mt * BM;
             const CUtensorMap* amap;
             const CUtensorMap* bmap;
             int b_row, k_blocks;
+            // second weight half (CL = 1 loads both halves itself)
+            const CUtensorMap* bmap2 = nullptr;
+            int b_row2 = 0;
             if (kind == 0) {
                 // gate/up: rank 0 loads the W1 (gate) rows, rank 1 the W3 (up) rows
+                // (one CTA: W1 rows, then W3 rows)
                 amap = &tmA1;
                 bmap = rank == 1 ? &tmB3 : &tmB1;
                 b_row = e * args.ffn + nt * (BN / 2);
+                bmap2 = &tmB3;
+                b_row2 = b_row;
                 k_blocks = args.k1;
             } else {
                 // down: rank r loads rows 128 r .. 128 r + 127 of the 256-row W2 tile
+                // (one CTA: both)
                 amap = &tmA2;
                 bmap = &tmB2;
                 b_row = e * args.d + nt * BN + rank * (BN / 2);
+                bmap2 = &tmB2;
+                b_row2 = b_row + BN / 2;
                 k_blocks = args.k2;
-                // its A rows are h rows of (e, mp): wait until every gate/up pair
-                // tile of them has been stored (four epilogue warps in each CTA)
+                // its A rows are h rows of (e, mp): wait until every gate/up
+                // tile of them has been stored (four epilogue warps per CTA)
                 const int* cnt = args.sync + 1 + (size_t)e * args.mp_cap + mp;
-                const int target = 4 * kCluster * n1;
+                const int target = 4 * CL * n1;
                 if (ld_acquire(cnt) < target) {
                     const uint64_t t0 = globaltimer();
                     while (ld_acquire(cnt) < target) {
@@ -432,11 +503,19 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
                     break;
                 }
                 const uint32_t sa = smem_u32(stages + (size_t)stage * STAGE_BYTES);
-                // the leader's full barrier counts both CTAs' bytes of the stage
-                const uint32_t fb = map_to_rank(smem_u32(&S.full[stage]), 0);
-                if (leader) mbar_arrive_expect_tx(smem_u32(&S.full[stage]), kCluster * STAGE_BYTES);
-                tma_load_2d_pair(sa, amap, fb, kb * BK, a_row);
-                tma_load_2d_pair(sa + A_BYTES, bmap, fb, kb * BK, b_row);
+                if constexpr (CL == 2) {
+                    // the leader's full barrier counts both CTAs' bytes of the stage
+                    const uint32_t fb = map_to_rank(smem_u32(&S.full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(smem_u32(&S.full[stage]), CL * STAGE_BYTES);
+                    tma_load_2d_pair(sa, amap, fb, kb * BK, a_row);
+                    tma_load_2d_pair(sa + A_BYTES, bmap, fb, kb * BK, b_row);
+                } else {
+                    const uint32_t fb = smem_u32(&S.full[stage]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    tma_load_2d_own(sa, amap, fb, kb * BK, a_row);
+                    tma_load_2d_own(sa + A_BYTES, bmap, fb, kb * BK, b_row);
+                    tma_load_2d_own(sa + A_BYTES + B_BYTES / 2, bmap2, fb, kb * BK, b_row2);
+                }
                 issued_parity[stage] = (int)phase;
                 if (++stage == STAGES) {
                     stage = 0;
@@ -453,14 +532,14 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
                 drain_phase(smem_u32(leader ? &S.full[s] : &S.empty[s]), (uint32_t)issued_parity[s], status);
     } else if (warp == 1 && lane == 0 && leader) {
         // ------------------------------------------------- MMA issuer --
-        constexpr uint32_t idesc = idesc_bf16(kCluster * BM, BN);
+        constexpr uint32_t idesc = idesc_bf16(CL * BM, BN);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int tile = cluster; tile < total_tiles; tile += nclusters) {
             int kind, e, mt, nt, mp;
-            tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
+            tile_coords<CL>(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
             const int k_blocks = kind == 0 ? args.k1 : args.k2;
             if (!wait_phase(smem_u32(&S.tempty[acc]), acc_phase ^ 1u, abort_flag, status)) break;
             tc_fence_after();
@@ -475,22 +554,30 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
                 const uint32_t sa = smem_u32(stages + (size_t)stage * STAGE_BYTES);
                 const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BK / UK; ++kk)
-                    mma_bf16_pair(d_tmem, sw128_desc(sa + kk * UK * 2), sw128_desc(sb + kk * UK * 2), idesc,
-                                  (kb | kk) != 0);
-                mma_commit_mc(smem_u32(&S.empty[stage]), kPairMask);
+                for (int kk = 0; kk < BK / UK; ++kk) {
+                    if constexpr (CL == 2)
+                        mma_bf16_pair(d_tmem, sw128_desc(sa + kk * UK * 2), sw128_desc(sb + kk * UK * 2), idesc,
+                                      (kb | kk) != 0);
+                    else
+                        mma_bf16_one(d_tmem, sw128_desc(sa + kk * UK * 2), sw128_desc(sb + kk * UK * 2), idesc,
+                                     (kb | kk) != 0);
+                }
+                if constexpr (CL == 2) mma_commit_mc(smem_u32(&S.empty[stage]), kPairMask);
+                else mma_commit_one(smem_u32(&S.empty[stage]));
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
             if (!ok) break;
-            mma_commit_mc(smem_u32(&S.tfull[acc]), kPairMask);
+            if constexpr (CL == 2) mma_commit_mc(smem_u32(&S.tfull[acc]), kPairMask);
+            else mma_commit_one(smem_u32(&S.tfull[acc]));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
         // every MMA this thread issued has completed once `drain` flips
-        mma_commit(smem_u32(&S.drain));
+        if constexpr (CL == 2) mma_commit(smem_u32(&S.drain));
+        else mma_commit_one(smem_u32(&S.drain));
         drain_phase(smem_u32(&S.drain), 0, status);
     } else if (warp >= 2) {
         // --------------------------------------------------- epilogue --
@@ -499,7 +586,7 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
         uint32_t acc_phase = 0;
         for (int tile = cluster; tile < total_tiles; tile += nclusters) {
             int kind, e, mt, nt, mp;
-            tile_coords(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
+            tile_coords<CL>(tile, S, n1, n2, rank, kind, e, mt, nt, mp);
             // every lane polls; the warp goes on only if all saw the tile done
             // (tcgen05.ld below needs the whole warp), so an abort that races
             // the phase cannot split it
@@ -508,7 +595,7 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
             tc_fence_after();
             const int rows_e = S.offs[e + 1] - S.offs[e];
             const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            uint8_t* stg = stages + kStgOffset + (size_t)q * kStgWarpBytes;
+            uint8_t* stg = stages + stg_offset<CL>() + (size_t)q * kStgWarpBytes;
             const int n_out = kind == 0 ? args.ffn : args.d;
             const int ncols = kind == 0 ? BN / 2 : BN;  // output columns of this tile
             const int col0 = nt * ncols;
@@ -565,7 +652,10 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(map_to_rank(smem_u32(&S.tempty[acc]), 0));
+            if (lane == 0) {
+                if constexpr (CL == 2) mbar_arrive_cluster(map_to_rank(smem_u32(&S.tempty[acc]), 0));
+                else mbar_arrive_local(smem_u32(&S.tempty[acc]));
+            }
             if (kind == 0) {
                 // release this warp's h rows to the down tiles that read them
                 __threadfence();
@@ -584,12 +674,17 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
     __syncthreads();
     // no CTA leaves (or frees tensor memory) while its peer may still read
     // its operands, write its accumulators or arrive on its barriers
-    cluster_sync();
+    if constexpr (CL == 2) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(TMEM_COLS)
-                     : "memory");
+        if constexpr (CL == 2)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(TMEM_COLS)
+                         : "memory");
     }
     // the last CTA out zeroes the release counters for the next launch
     if (threadIdx.x == 0) {
@@ -667,51 +762,85 @@ int num_sms() {
     return n;
 }
 
-// Cluster launch (pairs of CTAs) with programmatic dependent launch.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pairs(void (*kern)(KArgs...), unsigned clusters, cudaStream_t s, Args&&... args) {
+// Launch of form CL (clusters of CL CTAs) with programmatic dependent launch.
+template <int CL, typename... KArgs, typename... Args>
+cudaError_t launch_form(void (*kern)(KArgs...), unsigned clusters, cudaStream_t s, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(clusters * kCluster);
+    cfg.gridDim = dim3(clusters * CL);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes<CL>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = CL == 2 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Clusters of two that can be resident at once (one CTA per SM).
-int max_pairs() {
+// Clusters of form CL that can be resident at once (one CTA per SM).
+template <int CL>
+int max_clusters() {
     static const int n = []() {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(num_sms() / kCluster * kCluster));
-        cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kCluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
         int c = 0;
-        if (cudaOccupancyMaxActiveClusters(&c, tc_ffn_kernel, &cfg) != cudaSuccess || c <= 0)
-            c = num_sms() / kCluster;
+        if constexpr (CL == 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(num_sms() / CL * CL));
+            cfg.blockDim = dim3(kTcThreads);
+            cfg.dynamicSmemBytes = smem_bytes<CL>();
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = CL;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&c, tc_ffn_kernel<CL>, &cfg) != cudaSuccess || c <= 0)
+                c = num_sms() / CL;
+        } else {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_ffn_kernel<CL>, kTcThreads,
+                                                              smem_bytes<CL>()) != cudaSuccess ||
+                per_sm <= 0)
+                per_sm = 1;
+            c = per_sm * num_sms();
+        }
         return c;
     }();
     return n;
 }
 
+template <int CL>
+cudaError_t launch_ffn_form(const Problem& p, const CUtensorMap& mA1, const CUtensorMap& mB1, const CUtensorMap& mB3,
+                            const CUtensorMap& mA2, const CUtensorMap& mB2, FfnArgs a, cudaStream_t s) {
+    // per device, so set on every launch (a cheap host call)
+    cudaError_t e1 =
+        cudaFuncSetAttribute(tc_ffn_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<CL>());
+    if (e1 != cudaSuccess) return e1;
+    // upper bound of tile units over all experts: sum_e units(n_e) with
+    // m-tiles mt_e = ceil(n_e / BM), n_e <= C, sum_e mt_e <= ceil(rows_max / BM) + E
+    const int64_t mt_cap = ceil_div(p.C, BM);
+    const int64_t unit_cap = CL == 2 ? ceil_div(mt_cap, 2) : mt_cap;
+    const int64_t mt_total = ceil_div(p.rows_max, BM) + (int64_t)p.E;
+    const int64_t unit_bound =
+        std::min<int64_t>((int64_t)p.E * unit_cap, CL == 2 ? ceil_div(mt_total + (int64_t)p.E, 2) : mt_total);
+    a.mp_cap = (int)unit_cap;
+    // all clusters must be resident at once (down tiles wait on gate/up tiles
+    // of other clusters), so never more than the occupancy allows
+    const unsigned clusters =
+        (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_clusters<CL>(), unit_bound * (a.n1 + a.n2)));
+    return launch_form<CL>(tc_ffn_kernel<CL>, clusters, s, mA1, mB1, mB3, mA2, mB2, a);
+}
+
 }  // namespace
 
 size_t ffn_sync_ints(const Problem& p) {
+    // one counter per (expert, tile unit): m-tile pairs, or m-tiles for the
+    // one-CTA form (at most one per expert there)
     return 1 + (size_t)p.E * (size_t)ceil_div(ceil_div(p.C, BM), 2);
 }
 
@@ -727,15 +856,6 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
         !make_map(enc, &mB3, W3, E * p.ffn, p.d, BN / 2) || !make_map(enc, &mA2, h, rows, p.ffn, BM) ||
         !make_map(enc, &mB2, W2, E * p.d, p.ffn, BN / 2))
         return cudaErrorInvalidValue;
-
-    // per device, so set on every launch (a cheap host call)
-    cudaError_t e1 = cudaFuncSetAttribute(tc_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e1 != cudaSuccess) return e1;
-    // upper bound of m-tile pairs over all experts: sum_e ceil(mt_e / 2) with
-    // mt_e = ceil(n_e / BM), n_e <= C, sum_e mt_e <= ceil(rows_max / BM) + E
-    const int64_t mp_cap = ceil_div(ceil_div(p.C, BM), 2);
-    const int64_t mp_bound =
-        std::min<int64_t>((int64_t)p.E * mp_cap, ceil_div(ceil_div(p.rows_max, BM) + 2 * (int64_t)p.E, 2));
     FfnArgs a{};
     a.E = p.E;
     a.d = p.d;
@@ -745,7 +865,6 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
     a.k1 = (int)ceil_div(p.d, BK);
     a.n2 = (int)ceil_div(p.d, BN);
     a.k2 = (int)ceil_div(p.ffn, BK);
-    a.mp_cap = (int)mp_cap;
     a.expert_offsets = expert_offsets;
     a.h = (__nv_bfloat16*)h;
     a.yd = (__nv_bfloat16*)yd;
@@ -754,13 +873,11 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
     // Down tiles are several times longer than gate/up tiles (K = ffn vs d), so
     // they all go after the last gate/up tile: every cluster then ends on one
     // or two of them instead of a few clusters finishing the last expert's.
-    const int lag_tiles = 1 << 30;
-    // all clusters must be resident at once (down tiles wait on gate/up tiles
-    // of other clusters), so never more than the occupancy allows
-    const unsigned clusters =
-        (unsigned)std::max<int64_t>(1, std::min<int64_t>(max_pairs(), mp_bound * (a.n1 + a.n2)));
-    a.lag = lag_tiles;
-    return launch_pairs(tc_ffn_kernel, clusters, s, mA1, mB1, mB3, mA2, mB2, a);
+    a.lag = 1 << 30;
+    // one-CTA tiles when the capacity keeps every expert within one 128-row
+    // tile (a pair tile would be at least half padding); pairs otherwise
+    if (p.C <= BM) return launch_ffn_form<1>(p, mA1, mB1, mB3, mA2, mB2, a, s);
+    return launch_ffn_form<2>(p, mA1, mB1, mB3, mA2, mB2, a, s);
 }
 
 }  // namespace moe

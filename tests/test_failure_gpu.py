@@ -26,8 +26,13 @@ from tests.gpu_steps import Device, assert_close, host
 pytestmark = pytest.mark.gpu
 
 
-def test_ffn_release_wait_times_out_and_the_context_stays_usable():
-    wl = Workload("timeout_case", T=1000, d=256, E=8, D=4, k=2, ffn=384, capacity_factor=1.0, seed=91)
+@pytest.mark.parametrize("wl", [
+    # capacity 250: 2-SM pair tiles
+    Workload("timeout_pairs", T=1000, d=256, E=8, D=4, k=2, ffn=384, capacity_factor=1.0, seed=91),
+    # capacity 125: every expert within one 128-row tile, one-CTA tiles
+    Workload("timeout_single", T=1000, d=256, E=16, D=4, k=2, ffn=384, capacity_factor=1.0, seed=92),
+], ids=lambda w: w.name)
+def test_ffn_release_wait_times_out_and_the_context_stays_usable(wl):
     inp = moe_inputs.make_inputs(wl, device="cuda")
     dev = Device(inp)
     cpu = inp.to("cpu")
