@@ -65,11 +65,13 @@
 // histogram (one warp = 32 tokens = one assignment block), and the last CTA
 // scans it (assign_scan.cuh), or the slot-and-pack kernel does.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 tensor-memory
-// allocation and MMA issue, warps 2-5 the epilogue, one token per thread
-// (warp w reads tensor-memory lanes 32 * (w % 4) ..).  One accumulator set
-// per CTA: the stage ring (up to 10 stages) keeps loading the next tile while
-// the epilogue runs.  Every mbarrier wait is
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 tensor-memory
+// allocation and MMA issue, warps 2-9 the epilogue, two per tensor-memory lane
+// quarter (warp w reads lanes 32 * (w % 4) ..): the pair splits the quarter's
+// accumulator columns between them, meets on a shared-memory barrier, and then
+// each ranks 16 of the quarter's 32 tokens.  One accumulator set per CTA: the
+// stage ring (up to 10 stages) keeps loading the next tile while the epilogue
+// runs.  Every mbarrier wait is
 // bounded; on expiry the kernel records MOE_ERR_TIMEOUT's device bit, stops,
 // drains its own copies and MMAs (bounded), frees tensor memory and returns.
 #include <math_constants.h>
@@ -82,7 +84,8 @@ namespace {
 constexpr int kTM = 128;            // tokens per tile (MMA M)
 constexpr int kBK = 64;             // hidden elements per stage (one 128-byte swizzle row of bf16)
 constexpr int kUK = 16;             // K per MMA instruction
-constexpr int kRtThreads = 192;
+constexpr int kRtThreads = 320;
+constexpr int kEpiWarps = 8;       // two per tensor-memory lane quarter
 constexpr int kTmemCols = 512;
 // tensor-memory columns: x x^T at 0, the Wg Gram block at 128 (first tile
 // only), then the nc groups of partial logits (n_pad columns each)
@@ -105,10 +108,12 @@ struct __align__(8) RtShared {
     uint64_t tempty;
     uint64_t wdone;   // the epilogue warps' max ||Wg_e||^2 are in
     uint64_t drain;
+    uint64_t pair[4];  // the two epilogue warps of a lane quarter: table complete, then ranks stored
     uint32_t tmem_base;
     int abort_flag;
     float wmax_sq;   // max_e ||Wg_e||^2 (bit pattern max, values >= 0)
     float bias[256]; // the router bias (zero without one)
+    int sel[kTM * 8];  // the tile's chosen experts, token-major, k per token
 };
 
 struct RtArgs {
@@ -352,8 +357,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
             bar_init(s_u32(&sh.empty[s]), 1);
         }
         for (int j = 0; j < nc; ++j) bar_init(s_u32(&sh.gfull[j]), 1);
-        bar_init(s_u32(&sh.tempty), 4);
-        bar_init(s_u32(&sh.wdone), 4);
+        bar_init(s_u32(&sh.tempty), kEpiWarps);
+        bar_init(s_u32(&sh.wdone), kEpiWarps);
+        for (int j = 0; j < 4; ++j) bar_init(s_u32(&sh.pair[j]), 2);
         bar_init(s_u32(&sh.drain), 1);
         sh.abort_flag = 0;
         sh.wmax_sq = 0.0f;
@@ -447,10 +453,13 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
         bar_drain(s_u32(&sh.drain), 0, status);
     } else if (warp >= 2) {
         // --------------------------------------------------- epilogue --
-        const int q = warp & 3;  // tensor-memory lane quarter of this warp
+        const int q = warp & 3;          // tensor-memory lane quarter of this warp
+        const int half = (warp - 2) >> 2;  // which of the quarter's two warps
+        const bool own = (lane >> 4) == half;  // this lane's token is ranked by this warp
+        const uint32_t pair_bar = s_u32(&sh.pair[q]);
         const int E = a.E, k = a.k, d = a.d;
-        for (int e = threadIdx.x - 64; e < E; e += 128) sh.bias[e] = a.bias ? a.bias[e] : 0.0f;
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        for (int e = threadIdx.x - 64; e < E; e += 32 * kEpiWarps) sh.bias[e] = a.bias ? a.bias[e] : 0.0f;
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
         const float* bias = sh.bias;  // zero without a router bias
         const uint32_t lanes = (uint32_t)(q * 32) << 16;
         // logit table [n_pad][kLogitPitch]: expert-major, one column per token of
@@ -468,14 +477,15 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
 
             // the groups' partial logits, added into the table in ascending
             // group order as each group's MMAs complete (while later groups
-            // still stream in)
+            // still stream in); the pair's two warps take alternate 32-column
+            // blocks of the accumulator
             bool ok = true;
             for (int j = 0; j < nc && ok; ++j) {
                 ok = __all_sync(0xffffffffu, bar_wait(s_u32(&sh.gfull[j]), tphase, abort_flag, status));
                 if (!ok) break;
                 tc_after();
                 const uint32_t tg = tmem_base + lanes + (uint32_t)(kLogitCol0 + j * NP);
-                for (int c0 = 0; c0 < NP; c0 += 32) {
+                for (int c0 = 32 * half; c0 < NP; c0 += 64) {
                     float v0[16], v1[16];
                     tmem_ld16_nowait(tg + c0, v0);
                     if (c0 + 16 < NP) tmem_ld16_nowait(tg + c0 + 16, v1);
@@ -522,7 +532,10 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
             // accumulators are free for the next tile
             tc_before();
             __syncwarp();
-            if (lane == 0) bar_arrive(s_u32(&sh.tempty));
+            if (lane == 0) {
+                bar_arrive(s_u32(&sh.tempty));
+                bar_arrive(pair_bar);  // this warp's columns of the table are in
+            }
             if (first) {
                 // max_e ||Wg_e||^2 (rows past E hold x rows: excluded); the four
                 // warps' maxima meet on an mbarrier (a bounded wait, so a warp
@@ -538,8 +551,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 wmax = sqrtf(*reinterpret_cast<volatile float*>(&sh.wmax_sq) * a.gram_scale) * (1.0f + 1e-6f);
                 first = false;
             }
+            // the other warp's columns (two phases of the pair barrier per
+            // tile: 0 = table complete, 1 = ranks stored)
+            if (!__all_sync(0xffffffffu, bar_wait(pair_bar, 0, abort_flag, status))) break;
 
-            // the warp's 32 tokens, four at a time, lane = expert (expert
+            // the warp's 16 tokens, four at a time, lane = expert (expert
             // lane + 32 i): per token the k+1 largest g^ + b by repeated argmax
             // (a warp max of order-preserving bits, then the lowest expert
             // holding it), max |g^ + b|, and the softmax denominator over every
@@ -554,7 +570,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 le[i] = -1;
             }
             float maxabs = 0.0f, s_all = 0.0f;
-            for (int j0 = 0; j0 < 32; j0 += 4) {
+            for (int j0 = 16 * half; j0 < 16 * half + 16; j0 += 4) {
                 float v[4][kEPerLane];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -627,7 +643,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 if (r + 1 < K1) certain = certain && (lv[r] - lv[r + 1] > theta2);
                 if (r == k - 1) vk = lv[r];
             }
-            const bool redo = valid && !certain;
+            const bool redo = own && valid && !certain;
             // an uncertain token's candidates U: every expert within 2 theta of
             // its k-th largest
             const float band = vk - theta2;
@@ -680,7 +696,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 }
             }
 
-            if (valid) {
+            if (own && valid) {
                 const float inv = 1.0f / (s_all + s_exact);
                 float den = 0.0f;
 #pragma unroll
@@ -693,22 +709,30 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                         a.topk_gate[(size_t)t * k + r] = a.renorm ? expf(rv[r] - m) / den : expf(rv[r] - m) * inv;
                     }
             }
-            if (scan.hist && blk < scan.nblk) {
-                // this warp's 32 tokens are one assignment block: its per-(expert,
-                // rank) counts (zero for experts it does not choose)
+            if (own) {
+#pragma unroll
+                for (int r = 0; r < KM; ++r)
+                    if (r < k) sh.sel[row * KM + r] = valid ? re[r] : -1;
+            }
+            // both warps' ranks are stored, and both are done with the table
+            // (the next tile rewrites it only after this point)
+            __syncwarp();
+            if (lane == 0) bar_arrive(pair_bar);
+            if (!__all_sync(0xffffffffu, bar_wait(pair_bar, 1, abort_flag, status))) break;
+            if (half == 0 && scan.hist && blk < scan.nblk) {
+                // the quarter's 32 tokens are one assignment block: its
+                // per-(expert, rank) counts (zero for experts it does not choose)
                 for (int i = lane; i < E * k; i += 32) scan.hist[(size_t)i * scan.nblk + blk] = 0;
                 __syncwarp();
 #pragma unroll
                 for (int r = 0; r < KM; ++r)
                     if (r < k) {
-                        const int key = valid ? re[r] : -1;
+                        const int key = valid ? sh.sel[row * KM + r] : -1;
                         const uint32_t same = __match_any_sync(0xffffffffu, key);
                         if (valid && lane == __ffs(same) - 1)
                             scan.hist[((size_t)key * k + r) * scan.nblk + blk] = __popc(same);
                     }
             }
-            // the table is rewritten by the next tile only after every warp of
-            // this one is done with it (each warp owns its own token columns)
             __syncwarp();
             tphase ^= 1u;
         }
