@@ -307,18 +307,10 @@ __device__ __forceinline__ bool ranks_before(float v, int e, float lvp, int lep)
 // Insert (v, e) into such a list, keeping its first n entries (n <= L;
 // entries at n and beyond are not touched).  Unrolled so the list stays in
 // registers: entry p takes entry p-1 when (v, e) ranks before that one, else
-// (v, e) itself when it ranks before entry p.
+// (v, e) itself when it ranks before entry p; a value that ranks after entry
+// n-1 changes nothing.
 template <int L>
 __device__ __forceinline__ void list_insert(float (&lv)[L], int (&le)[L], int n, float v, int e) {
-    float tv = lv[0];
-    int te = le[0];
-#pragma unroll
-    for (int p = 1; p < L; ++p)
-        if (p == n - 1) {
-            tv = lv[p];
-            te = le[p];
-        }
-    if (!ranks_before(v, e, tv, te)) return;
 #pragma unroll
     for (int p = L - 1; p >= 0; --p) {
         if (p < n) {
@@ -332,7 +324,6 @@ __device__ __forceinline__ void list_insert(float (&lv)[L], int (&le)[L], int n,
         }
     }
 }
-
 
 // KM: largest k this instance serves
 template <int KM>
@@ -383,8 +374,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
         // ------------------------------------------------ TMA producer --
         int stage = 0;
         uint32_t phase = 0;
-        int issued_parity[kMaxStages];
-        for (int s = 0; s < kMaxStages; ++s) issued_parity[s] = -1;
+        // stages with a copy issued, and the phase parity of their last one
+        // (bit masks: an array indexed by the stage would live in local memory)
+        uint32_t issued = 0, issued_par = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             for (int c = 0; c < nchunks; ++c) {
@@ -397,7 +389,8 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 bar_expect_tx(fb, stage_bytes);
                 tma_2d(sb, &tmw, fb, c * kBK, 0);                                // Wg rows (zero past E)
                 tma_2d(sb + (uint32_t)NP * 128u, &tmx, fb, c * kBK, tile * kTM);  // x rows (zero past T)
-                issued_parity[stage] = (int)phase;
+                issued |= 1u << stage;
+                issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == S) {
                     stage = 0;
                     phase ^= 1u;
@@ -406,7 +399,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
         }
         // copies in flight land before the CTA leaves
         for (int s = 0; s < S; ++s)
-            if (issued_parity[s] >= 0) bar_drain(s_u32(&sh.full[s]), (uint32_t)issued_parity[s], status);
+            if ((issued >> s) & 1u) bar_drain(s_u32(&sh.full[s]), (issued_par >> s) & 1u, status);
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------- MMA issuer --
         int stage = 0;
@@ -605,11 +598,11 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                             const int be = (int)__reduce_min_sync(0xffffffffu,
                                                                   ob == om ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
                             const float val = from_order_bits(om);
-                            if ((be & 31) == lane) {
+                            // a select per entry: a store to v[u][be >> 5] would
+                            // put the token's values in local memory
 #pragma unroll
-                                for (int i = 0; i < kEPerLane; ++i)
-                                    if (i == (be >> 5)) v[u][i] = -CUDART_INF_F;
-                            }
+                            for (int i = 0; i < kEPerLane; ++i)
+                                v[u][i] = be == lane + 32 * i ? -CUDART_INF_F : v[u][i];
                             if (r == 0) top = val;
                             if (lane == j0 + u) {
                                 lv[r] = val;
@@ -635,13 +628,16 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
             const float m = lv[0];  // the largest g^ + b: the softmax shift
             const float xn = sqrtf(fmaxf(xsq, 0.0f) * a.gram_scale) * (1.0f + 1e-6f);
             const float theta2 = 2.0f * (a.c_d * xn * wmax + 2.4e-7f * maxabs);
-            // certain: the k+1 largest g^ are more than 2 theta apart; vk = the k-th
+            // certain: the k+1 largest g^ are more than 2 theta apart; vk = the
+            // k-th (the least of the k largest: the list is in descending order,
+            // and a minimum keeps the list out of local memory where lv[k - 1]
+            // would not)
             bool certain = true;
             float vk = lv[0];
 #pragma unroll
             for (int r = 0; r < KM; ++r) {
                 if (r + 1 < K1) certain = certain && (lv[r] - lv[r + 1] > theta2);
-                if (r == k - 1) vk = lv[r];
+                if (r < k) vk = fminf(vk, lv[r]);
             }
             const bool redo = own && valid && !certain;
             // an uncertain token's candidates U: every expert within 2 theta of
