@@ -63,34 +63,65 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int64_t L = (int64_t)a.k * a.nblk;
     // one warp per expert: exclusive scan of its k * nblk counts, in place,
-    // 256 entries per round (8 contiguous per lane, loads issued together)
-    for (int e = warp; e < a.E; e += nwarps) {
-        int32_t* h = a.hist + (size_t)e * L;
-        const int first_kept = a.second ? __ldcg(a.counts_kept + e) : 0;
-        int running = first_kept;
-        for (int64_t base = 0; base < L; base += 256) {
-            const int64_t i0 = base + 8 * lane;
-            int v[8];
+    // 256 entries (8 contiguous per lane) per chunk.  A warp's chunks, expert
+    // after expert, are read kScanDepth ahead of the one being scanned, so
+    // that many 1 KB reads per warp are in flight (the scan is otherwise
+    // bound by one L2 round trip per chunk).  Every entry is read before it
+    // is overwritten: chunk c is loaded while chunk c - kScanDepth is
+    // scanned, and stored only when its own turn comes.
+    constexpr int kScanDepth = 4;
+    const int nch = L > 0 ? (int)((L + 255) / 256) : 1;  // chunks per expert (an empty one still reports)
+    const int ncw = (warp < a.E ? (a.E - 1 - warp) / nwarps + 1 : 0) * nch;  // chunks of this warp
+    auto load_chunk = [&](int c, int (&v)[8]) {
+        if (c < ncw) {
+            const int e = warp + (c / nch) * nwarps;
+            const int64_t i0 = (int64_t)(c % nch) * 256 + 8 * lane;
+            const int32_t* h = a.hist + (size_t)e * L;
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = i0 + j < L ? __ldcg(h + i0 + j) : 0;
-            int loc = 0;
+        } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) loc += v[j];
-            int incl = loc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            int run = running + incl - loc;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (i0 + j < L) h[i0 + j] = run;
-                run += v[j];
-            }
-            running += __shfl_sync(0xffffffffu, incl, 31);
+            for (int j = 0; j < 8; ++j) v[j] = 0;
         }
-        if (lane == 0) {
+    };
+    int buf[kScanDepth][8];
+#pragma unroll
+    for (int q = 0; q < kScanDepth; ++q) load_chunk(q, buf[q]);
+    int running = 0, first_kept = 0;
+    for (int c = 0; c < ncw; ++c) {
+        int next[8];
+        load_chunk(c + kScanDepth, next);
+        const int e = warp + (c / nch) * nwarps;
+        const int ch = c % nch;
+        int32_t* h = a.hist + (size_t)e * L;
+        if (ch == 0) {
+            first_kept = a.second ? __ldcg(a.counts_kept + e) : 0;
+            running = first_kept;
+        }
+        const int64_t i0 = (int64_t)ch * 256 + 8 * lane;
+        int loc = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) loc += buf[0][j];
+        int incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = running + incl - loc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (i0 + j < L) h[i0 + j] = run;
+            run += buf[0][j];
+        }
+        running += __shfl_sync(0xffffffffu, incl, 31);
+#pragma unroll
+        for (int q = 0; q + 1 < kScanDepth; ++q)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) buf[q][j] = buf[q + 1][j];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) buf[kScanDepth - 1][j] = next[j];
+        if (ch == nch - 1 && lane == 0) {
             const int kept = (int)min((int64_t)running, a.C);
             const int routed = a.second ? __ldcg(a.counts_routed + e) : running;
             s_routed[e] = routed;
