@@ -95,6 +95,7 @@ constexpr int kLogitCol0 = 256;
 constexpr int kMaxGroups = 16;
 constexpr int kLogitPitch = kTM + 1;  // floats per expert row of the epilogue's logit table
 constexpr int kEPerLane = 4;          // experts per lane when a warp walks one token (E <= 128)
+constexpr int kTokPar = 4;            // tokens a warp ranks side by side
 constexpr int kMaxStages = 10;
 constexpr int kStageBudget = 200 * 1024;      // shared memory for the stage ring and the logit table
 constexpr uint64_t kTcTimeoutNs = 2000000000ull;  // 2 s: far above any legitimate wait
@@ -563,67 +564,96 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__
                 le[i] = -1;
             }
             float maxabs = 0.0f, s_all = 0.0f;
-            for (int j0 = 16 * half; j0 < 16 * half + 16; j0 += 4) {
-                float v[4][kEPerLane];
+            // Each step below is written for kTokPar tokens side by side, so
+            // that their warp reductions are independent neighbours in the
+            // instruction stream and overlap (one token's chain alone is a
+            // row of dependent reductions).
+            for (int j0 = 16 * half; j0 < 16 * half + 16; j0 += kTokPar) {
+                float v[kTokPar][kEPerLane];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < kTokPar; ++u)
 #pragma unroll
                     for (int i = 0; i < kEPerLane; ++i) {
                         const int e = lane + 32 * i;
                         // + 0.0f turns -0 into +0, so order-preserving bits tie as the values do
                         v[u][i] = e < E ? gt[e * kLogitPitch + q * 32 + j0 + u] + bias[e] + 0.0f : -CUDART_INF_F;
                     }
+                float la[kTokPar];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float la = 0.0f;
+                for (int u = 0; u < kTokPar; ++u) {
+                    la[u] = 0.0f;
 #pragma unroll
                     for (int i = 0; i < kEPerLane; ++i)
-                        if (lane + 32 * i < E) la = fmaxf(la, fabsf(v[u][i]));
-                    la = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(la)));
-                    float top = 0.0f;
+                        if (lane + 32 * i < E) la[u] = fmaxf(la[u], fabsf(v[u][i]));
+                }
 #pragma unroll
-                    for (int r = 0; r <= KM; ++r) {
-                        if (r < K1) {
-                            // this lane's largest remaining value (lower expert first)
+                for (int u = 0; u < kTokPar; ++u)
+                    la[u] = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(la[u])));
+                float top[kTokPar];
+#pragma unroll
+                for (int r = 0; r <= KM; ++r) {
+                    if (r < K1) {
+                        // each token: this lane's largest remaining value (lower
+                        // expert first), then the warp's largest and the lowest
+                        // expert holding it
+                        uint32_t ob[kTokPar], om[kTokPar];
+                        int bi[kTokPar], be[kTokPar];
+#pragma unroll
+                        for (int u = 0; u < kTokPar; ++u) {
                             float bv = -CUDART_INF_F;
-                            int bi = 0;
+                            bi[u] = 0;
 #pragma unroll
                             for (int i = 0; i < kEPerLane; ++i)
                                 if (v[u][i] > bv) {
                                     bv = v[u][i];
-                                    bi = i;
+                                    bi[u] = i;
                                 }
-                            const uint32_t ob = order_bits(bv);
-                            const uint32_t om = __reduce_max_sync(0xffffffffu, ob);
-                            const int be = (int)__reduce_min_sync(0xffffffffu,
-                                                                  ob == om ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
-                            const float val = from_order_bits(om);
+                            ob[u] = order_bits(bv);
+                        }
+#pragma unroll
+                        for (int u = 0; u < kTokPar; ++u) om[u] = __reduce_max_sync(0xffffffffu, ob[u]);
+#pragma unroll
+                        for (int u = 0; u < kTokPar; ++u)
+                            be[u] = (int)__reduce_min_sync(0xffffffffu,
+                                                           ob[u] == om[u] ? (uint32_t)(lane + 32 * bi[u]) : 0xffffffffu);
+#pragma unroll
+                        for (int u = 0; u < kTokPar; ++u) {
+                            const float val = from_order_bits(om[u]);
                             // a select per entry: a store to v[u][be >> 5] would
                             // put the token's values in local memory
 #pragma unroll
                             for (int i = 0; i < kEPerLane; ++i)
-                                v[u][i] = be == lane + 32 * i ? -CUDART_INF_F : v[u][i];
-                            if (r == 0) top = val;
+                                v[u][i] = be[u] == lane + 32 * i ? -CUDART_INF_F : v[u][i];
+                            if (r == 0) top[u] = val;
                             if (lane == j0 + u) {
                                 lv[r] = val;
-                                le[r] = be;
+                                le[r] = be[u];
                             }
                         }
                     }
-                    // the removed entries are restored from the table for the sum
-                    float sum = 0.0f;
+                }
+                // the denominators (the removed entries are restored from the
+                // table), then one xor butterfly for all of them
+                float sum[kTokPar];
+#pragma unroll
+                for (int u = 0; u < kTokPar; ++u) {
+                    sum[u] = 0.0f;
 #pragma unroll
                     for (int i = 0; i < kEPerLane; ++i) {
                         const int e = lane + 32 * i;
-                        if (e < E) sum += __expf(gt[e * kLogitPitch + q * 32 + j0 + u] + bias[e] - top);
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                    if (lane == j0 + u) {
-                        maxabs = la;
-                        s_all = sum;
+                        if (e < E) sum[u] += __expf(gt[e * kLogitPitch + q * 32 + j0 + u] + bias[e] - top[u]);
                     }
                 }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int u = 0; u < kTokPar; ++u) sum[u] += __shfl_xor_sync(0xffffffffu, sum[u], o);
+#pragma unroll
+                for (int u = 0; u < kTokPar; ++u)
+                    if (lane == j0 + u) {
+                        maxabs = la[u];
+                        s_all = sum[u];
+                    }
             }
             const float m = lv[0];  // the largest g^ + b: the softmax shift
             const float xn = sqrtf(fmaxf(xsq, 0.0f) * a.gram_scale) * (1.0f + 1e-6f);
