@@ -259,8 +259,8 @@ int moe_layer_forward(const moe_problem* p, const void* x, const void* Wg, const
  * token, the same FFN form as the routed experts (p->act) with width
  * p->ffn_shared (> 0).  Ws1, Ws3: [ffn_shared, d] (Ws3 NULL for GELU);
  * Ws2: [d, ffn_shared]; ys: [T, d] in the layer dtype.  bf16 SwiGLU runs on
- * the same 2-SM tensor-core FFN kernel as the routed experts (one expert
- * whose rows are x's rows).  Uses the workspace's hs and shared_sync regions. */
+ * the same tensor-core FFN kernel as the routed experts (one expert whose
+ * rows are x's rows).  Uses the workspace's hs and shared_sync regions. */
 int moe_shared_expert_ffn(const moe_problem* p, const void* x, const void* Ws1, const void* Ws3,
                           const void* Ws2, void* ys, void* ws, size_t ws_bytes, void* stream);
 
