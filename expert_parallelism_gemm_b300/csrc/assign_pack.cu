@@ -54,30 +54,32 @@ assign_pack_kernel(int64_t Tn, int d, const T* __restrict__ x, const int32_t* __
     for (int64_t i = tid; i < n; i += kThreads) sh[i] = __ldcg(a.hist + i);
     __syncthreads();
     // 1. per expert: exclusive prefixes in (r, b) order, 256 entries a round
+    //    held as 8 rows of 32 (entry 32 j + lane in v[j]: conflict-free in
+    //    shared memory), each row scanned across the lanes, the rows' totals
+    //    added in row order
     for (int e = warp; e < E; e += kWarpsHere) {
         int* h = sh + (int64_t)e * L;
         int running = 0;
         for (int64_t base = 0; base < L; base += 256) {
-            const int64_t i0 = base + 8 * lane;
-            int v[8], loc = 0;
+            const int64_t i0 = base + lane;
+            int v[8], incl[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                v[j] = i0 + j < L ? h[i0 + j] : 0;
-                loc += v[j];
+                v[j] = i0 + 32 * j < L ? h[i0 + 32 * j] : 0;
+                incl[j] = v[j];
             }
-            int incl = loc;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int m = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += m;
-            }
-            int run = running + incl - loc;
+            for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int m = __shfl_up_sync(0xffffffffu, incl[j], o);
+                    if (lane >= o) incl[j] += m;
+                }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                if (i0 + j < L) h[i0 + j] = run;
-                run += v[j];
+                if (i0 + 32 * j < L) h[i0 + 32 * j] = running + incl[j] - v[j];
+                running += __shfl_sync(0xffffffffu, incl[j], 31);
             }
-            running += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) s_routed[e] = running;
     }

@@ -48,6 +48,9 @@ struct AssignScan {
 // Call from every thread of every CTA after the CTA's hist entries are
 // written (no thread may have returned early).  Works for any block size
 // that is a multiple of 32.
+// kScanDepth: histogram chunks each warp reads ahead of the one it scans
+// (registers: 8 per chunk per thread; 0 reads each chunk just before its scan).
+template <int kScanDepth = 4>
 __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
     __shared__ bool s_last;
     __shared__ int s_routed[256];
@@ -63,64 +66,72 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const int64_t L = (int64_t)a.k * a.nblk;
     // one warp per expert: exclusive scan of its k * nblk counts, in place,
-    // 256 entries (8 contiguous per lane) per chunk.  A warp's chunks, expert
-    // after expert, are read kScanDepth ahead of the one being scanned, so
-    // that many 1 KB reads per warp are in flight (the scan is otherwise
-    // bound by one L2 round trip per chunk).  Every entry is read before it
-    // is overwritten: chunk c is loaded while chunk c - kScanDepth is
-    // scanned, and stored only when its own turn comes.
-    constexpr int kScanDepth = 4;
+    // 256 entries per chunk held as 8 rows of 32 (entry 32 j + lane of the
+    // chunk in v[j]), so every load and store of a warp covers 128
+    // contiguous bytes.  Each row is scanned across the lanes, two rows at a
+    // time packed in the halves of one word: an entry counts the tokens of
+    // one 32-token block, so a row's prefixes stay below 2^16.  The rows'
+    // totals are then added in row order.  A warp's chunks, expert after
+    // expert, are read kScanDepth ahead of the one being scanned.  Every
+    // entry is read before it is overwritten: chunk c is loaded while chunk
+    // c - kScanDepth is scanned, and stored only when its own turn comes.
+    static_assert(kAssignBlock * 32 < (1 << 16), "row prefixes must fit 16 bits");
     const int nch = L > 0 ? (int)((L + 255) / 256) : 1;  // chunks per expert (an empty one still reports)
     const int ncw = (warp < a.E ? (a.E - 1 - warp) / nwarps + 1 : 0) * nch;  // chunks of this warp
-    auto load_chunk = [&](int c, int (&v)[8]) {
-        if (c < ncw) {
-            const int e = warp + (c / nch) * nwarps;
-            const int64_t i0 = (int64_t)(c % nch) * 256 + 8 * lane;
-            const int32_t* h = a.hist + (size_t)e * L;
+    // the next chunk to read: its expert and index within the expert
+    int ld_e = warp, ld_ch = 0, ld_c = 0;
+    auto load_next = [&](int (&v)[8]) {
+        if (ld_c < ncw) {
+            const int64_t i0 = (int64_t)ld_ch * 256 + lane;
+            const int32_t* h = a.hist + (size_t)ld_e * L;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = i0 + j < L ? __ldcg(h + i0 + j) : 0;
+            for (int j = 0; j < 8; ++j) v[j] = i0 + 32 * j < L ? __ldcg(h + i0 + 32 * j) : 0;
+            ++ld_c;
+            if (++ld_ch == nch) {
+                ld_ch = 0;
+                ld_e += nwarps;
+            }
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) v[j] = 0;
         }
     };
-    int buf[kScanDepth][8];
+    int buf[kScanDepth + 1][8];
 #pragma unroll
-    for (int q = 0; q < kScanDepth; ++q) load_chunk(q, buf[q]);
+    for (int q = 0; q < kScanDepth; ++q) load_next(buf[q]);
     int running = 0, first_kept = 0;
+    int e = warp, ch = 0;  // the chunk being scanned
     for (int c = 0; c < ncw; ++c) {
-        int next[8];
-        load_chunk(c + kScanDepth, next);
-        const int e = warp + (c / nch) * nwarps;
-        const int ch = c % nch;
+        load_next(buf[kScanDepth]);
         int32_t* h = a.hist + (size_t)e * L;
         if (ch == 0) {
             first_kept = a.second ? __ldcg(a.counts_kept + e) : 0;
             running = first_kept;
         }
-        const int64_t i0 = (int64_t)ch * 256 + 8 * lane;
-        int loc = 0;
+        const int64_t i0 = (int64_t)ch * 256 + lane;
+        uint32_t pk[4];  // rows j and j + 4
 #pragma unroll
-        for (int j = 0; j < 8; ++j) loc += buf[0][j];
-        int incl = loc;
+        for (int j = 0; j < 4; ++j) pk[j] = (uint32_t)buf[0][j] | ((uint32_t)buf[0][j + 4] << 16);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
-        }
-        int run = running + incl - loc;
+        for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t n = __shfl_up_sync(0xffffffffu, pk[j], o);
+                if (lane >= o) pk[j] += n;
+            }
+        uint32_t tot[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) tot[j] = __shfl_sync(0xffffffffu, pk[j], 31);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            if (i0 + j < L) h[i0 + j] = run;
-            run += buf[0][j];
+            const int incl = (int)(j < 4 ? pk[j] & 0xffffu : pk[j - 4] >> 16);
+            if (i0 + 32 * j < L) h[i0 + 32 * j] = running + incl - buf[0][j];
+            running += (int)(j < 4 ? tot[j] & 0xffffu : tot[j - 4] >> 16);
         }
-        running += __shfl_sync(0xffffffffu, incl, 31);
 #pragma unroll
-        for (int q = 0; q + 1 < kScanDepth; ++q)
+        for (int q = 0; q < kScanDepth; ++q)
 #pragma unroll
             for (int j = 0; j < 8; ++j) buf[q][j] = buf[q + 1][j];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) buf[kScanDepth - 1][j] = next[j];
         if (ch == nch - 1 && lane == 0) {
             const int kept = (int)min((int64_t)running, a.C);
             const int routed = a.second ? __ldcg(a.counts_routed + e) : running;
@@ -129,6 +140,10 @@ __device__ __forceinline__ void finish_assign_scan(const AssignScan& a) {
             s_moved[e] = kept - first_kept;
             if (!a.second) a.counts_routed[e] = routed;
             a.counts_kept[e] = kept;
+        }
+        if (++ch == nch) {
+            ch = 0;
+            e += nwarps;
         }
     }
     __syncthreads();

@@ -461,7 +461,9 @@ route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CU
             const int e = i / k, r = i % k;
             scan.hist[((size_t)e * k + r) * scan.nblk + b] = cnt[r * E + e];
         }
-        if (!scan.defer) finish_assign_scan(scan);
+        // histogram reads kept ahead of the scan: two for bf16, none for fp32
+        // (whose 16-expert instance would spill under the 128-register cap)
+        if (!scan.defer) finish_assign_scan<sizeof(T) == 2 ? 2 : 0>(scan);
     }
 }
 
