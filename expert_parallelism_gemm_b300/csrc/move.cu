@@ -16,8 +16,9 @@
 // Both are HBM-bound copies: one warp per row or token, each lane moving 16
 // bytes per access, so a warp touches 512 contiguous bytes per instruction.
 // Each lane issues a batch of loads (4 vectors for dispatch; for combine, the
-// k source rows of up to 4 vector columns, plus the residual) before it
-// consumes any, so several loads per lane are in flight.
+// k source rows of 2 vector columns, 1 for k > 2, plus the shared expert's
+// output and the residual) before it consumes any, so several loads per lane
+// are in flight.
 #include "common.cuh"
 
 namespace moe {
@@ -55,17 +56,18 @@ dispatch_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restrict_
     }
 }
 
-// CB vector columns per lane per step, each gathering up to 8 / CB ranks, so
-// all of a step's loads are issued before the first multiply-add.
-template <typename T, int CB>
+// CB vector columns per lane per step, each gathering up to KM ranks, so all
+// of a step's loads are issued before the first multiply-add.  CB * KM is
+// kept at 4 or 8 vectors: more would hold the kernel to two CTAs per SM by
+// its registers, and a warp's one token per pass leaves it latency-bound.
+template <typename T, int CB, int KM>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __restrict__ yd,
                const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_pos,
                const int32_t* __restrict__ expert_offsets, const float* __restrict__ topk_gate,
                const T* __restrict__ shared, const T* __restrict__ residual, T* __restrict__ y) {
     dep_wait();
-    constexpr int VE = vec_elems<T>();
-    constexpr int KM = 8 / CB;  // ranks this instantiation handles (k <= KM)
+    constexpr int VE = vec_elems<T>();  // KM: ranks this instantiation handles (k <= KM)
     const int nv = d / VE;
     const int lane = threadIdx.x & 31;
     for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < Tn;
@@ -161,7 +163,7 @@ cudaError_t launch_combine_t(const Problem& p, unsigned g, const void* yd, const
     const T* st = (const T*)shared;
     const T* rt = (const T*)residual;
     T* yt = (T*)y;
-    auto kern = p.k <= 2 ? combine_kernel<T, 4> : p.k <= 4 ? combine_kernel<T, 2> : combine_kernel<T, 1>;
+    auto kern = p.k <= 2 ? combine_kernel<T, 2, 2> : p.k <= 4 ? combine_kernel<T, 1, 4> : combine_kernel<T, 1, 8>;
     return launch_k(kern, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d, p.k, ydt, topk_idx,
                     slot_pos, expert_offsets, topk_gate, st, rt, yt);
 }
