@@ -50,6 +50,10 @@ SMALL = {
                              capacity_factor=0.01, seed=17),
     "k8_e16": Workload("k8_e16", T=200, d=64, E=16, D=4, k=8, ffn=64, capacity_factor=1.0, seed=18),
     "e256": Workload("e256", T=300, d=64, E=256, D=8, k=2, ffn=64, capacity_factor=2.0, seed=19),
+    # capacity 157 rows with a mean load of 125: the one-CTA FFN form with up to
+    # two 128-row tiles per expert
+    "thin_two_tiles": Workload("thin_two_tiles", T=1000, d=256, E=16, D=4, k=2, ffn=384,
+                               capacity_factor=1.25, seed=25),
     "hot_expert": Workload("hot_expert", T=700, d=128, E=8, D=4, k=2, ffn=128,
                            capacity_factor=1.0, seed=22, zipf_s=6.0),
     "tiny_fp32": moe_inputs.WORKLOADS["tiny_fp32"],
