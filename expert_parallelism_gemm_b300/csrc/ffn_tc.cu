@@ -14,7 +14,8 @@
 //            gate columns and the 128 matching up columns)
 //   down:    yd[r, :] = h[r] W2[e]^T
 // from one tile list: each expert's gate/up tiles, then -- once `lag` more
-// tiles (two waves of clusters) have been placed -- its down tiles.  A down
+// tiles have been placed -- its down tiles (the launcher sets `lag` past the
+// end of the list, so every down tile follows the last gate/up tile).  A down
 // tile reads h rows of one (expert, m-tile pair); its producer waits (bounded,
 // acquire) until the four epilogue warps of both CTAs of every gate/up tile
 // of that pair have stored their rows and released a counter, then issues its
@@ -36,11 +37,12 @@
 // part in its pair's loads and MMAs and stores nothing.
 //
 // When the capacity keeps every expert within one 128-row tile (C <= 128, as
-// in layers of many small experts), a pair tile would be at least half
-// padding; the kernel then runs in its one-CTA form instead: no clusters,
-// 128 x 256 tiles with the one-SM MMA (tcgen05.mma.cta_group::1, M = 128),
-// each CTA loading its A tile and the whole 256-row weight tile (4 stages of
-// 48 KB), release counters per (expert, m-tile).  Everything else is shared.
+// in layers of many small experts), or within two while the mean load per
+// expert fits one, most pair tiles would be half padding; the kernel then
+// runs in its one-CTA form instead: no clusters, 128 x 256 tiles with the
+// one-SM MMA (tcgen05.mma.cta_group::1, M = 128), each CTA loading its A tile
+// and the whole 256-row weight tile (4 stages of 48 KB), release counters per
+// (expert, m-tile).  Everything else is shared.
 //
 // Per CTA (one per SM, 192 threads):
 //   warp 0   TMA producer: its A tile [128 x 64] and its B half [128 x 64]
