@@ -659,8 +659,10 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
                 else mbar_arrive_local(smem_u32(&S.tempty[acc]));
             }
             if (kind == 0) {
-                // release this warp's h rows to the down tiles that read them
-                __threadfence();
+                // release this warp's h rows to the down tiles that read them:
+                // the warp barrier orders every lane's stores before lane 0's
+                // release-add (gpu scope), whose release covers them, so the
+                // consumer's acquire of the counter sees all 32 lanes' rows
                 __syncwarp();
                 if (lane == 0)
                     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(
