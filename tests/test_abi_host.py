@@ -118,7 +118,7 @@ def test_workspace_layout_is_aligned_and_disjoint():
                      shard_offsets=4 * (wl.D + 1), shard_routed=4 * wl.D, shard_overflow=4 * wl.D,
                      dropped=4, hist=4 * wl.E * wl.k * nblk, row_token=4 * rows_max,
                      xd=eb * rows_max * wl.d, h=eb * rows_max * wl.ffn, yd=eb * rows_max * wl.d,
-                     ffn_sync=4 * (1 + wl.E * -(-C // 128)),
+                     ffn_sync=4 * (2 + wl.E * -(-C // 128)),
                      stats=8 * (wl.E + 1))
         spans = sorted((L[n], L[n] + s) for n, s in sizes.items())
         # rerouting adds the fallback choices (and the rerouted count) to the same layout

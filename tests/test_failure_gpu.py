@@ -45,13 +45,14 @@ def test_ffn_release_wait_times_out_and_the_context_stays_usable(wl):
     xd = xd.cuda()
     offs = torch.from_numpy(s.expert_offsets).cuda()
 
-    # the region holds a counter per (expert, 128-row m-tile); the pair form
-    # uses one per (expert, m-tile pair), the one-CTA form (capacity within
-    # one tile, or within two with a mean load within one) one per m-tile
+    # the region holds the exit ticket, a counter per (expert, 128-row m-tile)
+    # and the progress window; the pair form uses one counter per (expert,
+    # m-tile pair), the one-CTA form (capacity within one tile, or within two
+    # with a mean load within one) one per m-tile
     m_tiles = -(-dev.C // 128)
     one_cta = dev.C <= 128 or (dev.C <= 256 and wl.T * wl.k <= wl.E * 128)
     n_used = 1 + wl.E * (m_tiles if one_cta else -(-m_tiles // 2))
-    sync = dev.region("ffn_sync", torch.int32, 1 + wl.E * m_tiles)
+    sync = dev.region("ffn_sync", torch.int32, 2 + wl.E * m_tiles)
     assert int(sync.abs().sum()) == 0
     sync[1:n_used] = -(1 << 30)  # release counters that can never reach their target
     torch.cuda.synchronize()
