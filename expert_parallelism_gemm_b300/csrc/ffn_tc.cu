@@ -478,11 +478,13 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
         // at its k-th tile, t = cluster + k * nclusters, every cluster has
         // issued at least k tiles, so the count is at least k * nclusters >
         // t - nclusters.  A narrower window could leave it waiting.
-        // Short launches (under 32 tiles per cluster) cannot drift far and
-        // run without the window (the Mixtral-style layer, 16 tiles per
-        // cluster: 133 -> 131 us).
+        // Short launches (under 32 tiles per cluster) cannot drift far, and
+        // layers whose experts hold at most a few tile units (capacity under 8
+        // units) have little A to share; both run without the window (the
+        // Mixtral-style layer, 16 tiles per cluster: 133 -> 131 us; the
+        // 128-expert layers at capacity 160-256 rows lost 2% with it).
         int* const progress = args.sync + 1 + (size_t)args.E * args.mp_cap;
-        const int window = total_tiles >= 32 * nclusters ? nclusters : total_tiles;
+        const int window = total_tiles >= 32 * nclusters && args.mp_cap >= 8 ? nclusters : total_tiles;
         for (int tile = cluster; tile < total_tiles && !*abort_flag; tile += nclusters) {
             if (leader && tile >= window && ld_acquire(progress) < tile - window) {
                 const uint64_t t0 = globaltimer();
