@@ -292,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- a shared expert as wide as a routed one over every token (the
     # layer option of moe_layer_forward_shared), timed alone like the calls
-    shared_ms = None
+    shared_ms = shared_layer_ms = None
     if wl.dtype == "bf16" and wl.act == "swiglu":
         swl = wl.with_(ffn_shared=wl.ffn)
         sp = moe.problem_of(swl)
@@ -318,7 +318,29 @@ def run_ours(args, rank, world, local_rank):
         shared_ms = statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in sh_ev)
         if moe.moe_device_status(sws, stream) != moe.MOE_OK:
             raise RuntimeError("device status after the shared-expert loop")
-        del sin, sws, ys
+        # the whole layer with that shared expert (its FFN overlaps the routed
+        # FFN's last tiles), against the routed layer and the shared FFN apart
+        ys_layer = torch.empty(wl.T, wl.d, dtype=inp.x.dtype, device=dev)
+        shl_fn = lambda: moe.moe_layer_forward_shared(sp, sin.x, sin.Wg, sin.bias, sin.W1, sin.W3, sin.W2, sin.Ws1,
+                                                      sin.Ws3, sin.Ws2, None, ys_layer, sws, sws.numel(), None)
+        shl_fn()
+        torch.cuda.synchronize(dev)
+        g_shl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_shl):
+            shl_fn()
+        shl_ev = []
+        for _ in range(args.steps):
+            flush()
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(stream)
+            g_shl.replay()
+            b_ev.record(stream)
+            shl_ev.append((a_ev, b_ev))
+        torch.cuda.synchronize(dev)
+        shared_layer_ms = statistics.mean(a_ev.elapsed_time(b_ev) for a_ev, b_ev in shl_ev)
+        if moe.moe_device_status(sws, stream) != moe.MOE_OK:
+            raise RuntimeError("device status after the shared-layer loop")
+        del sin, sws, ys, ys_layer, g_sh, g_shl
 
     def time_layer_variant(vwl, what):
         """One whole moe_layer_forward of a layer variant per graph replay;
@@ -454,7 +476,9 @@ def run_ours(args, rank, world, local_rank):
             "shared_expert_ffn": None if shared_ms is None else {
                 "ms": shared_ms, "ffn_shared": wl.ffn,
                 "TFLOP_s": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / 1e12,
-                "frac_bf16": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / (bf16_tf * 1e12)},
+                "frac_bf16": 2.0 * mats * wl.d * wl.ffn * wl.T / (shared_ms * 1e-3) / (bf16_tf * 1e12),
+                "layer_ms": shared_layer_ms,
+                "note": "ms: moe_shared_expert_ffn alone; layer_ms: moe_layer_forward_shared, graph replay"},
             "expert_choice_layer": {"ms": ec_ms, "tokens_per_s": wl.T / (ec_ms * 1e-3), "rows": ec_rows,
                                     "note": "whole moe_layer_forward with expert-choice routing, graph replay"},
             "reroute_layer": None if rr_ms is None else dict(

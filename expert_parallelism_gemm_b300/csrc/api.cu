@@ -143,15 +143,16 @@ int check_ws(const Problem& p, void* ws, size_t ws_bytes, moe_workspace_layout* 
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-// The shared expert's FFN over all T tokens (rows of x in order) into ys.
+// The shared expert's FFN over all T tokens (rows of x in order) into ys;
+// `order`: FfnOrder bits of its tensor-core launch.
 int run_shared_expert(const Problem& p, const moe_workspace_layout& L, char* w, const void* x, const void* Ws1,
-                      const void* Ws3, const void* Ws2, void* ys, cudaStream_t s) {
+                      const void* Ws3, const void* Ws2, void* ys, cudaStream_t s, int order = 0) {
     const Problem sp = shared_problem(p);
     void* hs = w + L.hs;
     int* status = (int*)(w + L.status);
     cudaError_t e;
     if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
-        e = launch_ffn_tc(sp, x, nullptr, Ws1, Ws3, Ws2, hs, ys, status, (int*)(w + L.shared_sync), s);
+        e = launch_ffn_tc(sp, x, nullptr, Ws1, Ws3, Ws2, hs, ys, status, (int*)(w + L.shared_sync), s, order);
         if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
     } else {
         e = launch_ffn_simt(sp, x, nullptr, Ws1, Ws3, Ws2, hs, ys, s);
@@ -229,9 +230,16 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
         }
     }
     if (e == cudaSuccess && !packed) e = launch_dispatch(p, x, row_token, off, xd, s);
+    // With a shared expert (tensor-core form) the routed FFN lets the shared
+    // expert's FFN launch as its CTAs run out of tiles, and the shared FFN --
+    // which reads only x and its weights and writes only its own hs, ys and
+    // counters -- waits for the routed one at its end: its CTAs fill the SMs
+    // of the routed launch's tail, and the combine still starts after both.
+    const bool overlap_shared = has_shared && p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU && p.rows_max > 0;
     if (e == cudaSuccess) {
         if (p.dtype == MOE_BF16 && p.act == MOE_ACT_SWIGLU) {
-            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, (int*)(w + L.ffn_sync), s);
+            e = launch_ffn_tc(p, xd, off, W1, W3, W2, h, yd, status, (int*)(w + L.ffn_sync), s,
+                              overlap_shared ? kFfnReleaseNext : 0);
             if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
         } else {
             e = launch_ffn_simt(p, xd, off, W1, W3, W2, h, yd, s);
@@ -239,7 +247,7 @@ int layer_forward(const moe_problem* mp, const void* x, const void* Wg, const fl
     }
     void* ys = has_shared ? (void*)(w + L.ys) : nullptr;
     if (e == cudaSuccess && has_shared) {
-        const int rc2 = run_shared_expert(p, L, w, x, Ws1, Ws3, Ws2, ys, s);
+        const int rc2 = run_shared_expert(p, L, w, x, Ws1, Ws3, Ws2, ys, s, overlap_shared ? kFfnWaitAtEnd : 0);
         if (rc2 != MOE_OK) return rc2;
     }
     if (e == cudaSuccess)

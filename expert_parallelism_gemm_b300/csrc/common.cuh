@@ -231,9 +231,22 @@ bool encode_row_tiles(CUtensorMap* m, const void* base, int dtype, uint64_t rows
 // when the tensor-map encoder cannot be obtained.
 // `sync` is the workspace's ffn_sync region (ffn_sync_ints(p) ints, zero
 // before the first launch; each launch leaves it zero again).
+// `order` (FfnOrder bits) relaxes the launch's ordering against its neighbours
+// on the stream:
+//  - kFfnReleaseNext: every CTA lets the next kernel launch once it has issued
+//    its last tile's loads (griddepcontrol.launch_dependents), so that kernel's
+//    CTAs take the SMs this launch's CTAs leave while its last tiles finish;
+//  - kFfnWaitAtEnd: the launch waits for the previous kernel at its end instead
+//    of its start.  Only for a launch that reads nothing the kernels before it
+//    in the stream write or still read, and that follows a kernel all of whose
+//    CTAs wait for their own predecessor before they let it launch (every
+//    kernel of this library): then all earlier kernels but that one are done,
+//    and the wait at the end keeps the kernel after this one from starting
+//    before that one completes.
+enum FfnOrder : int { kFfnReleaseNext = 1, kFfnWaitAtEnd = 2 };
 cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
                           const void* W1, const void* W3, const void* W2, void* h, void* yd,
-                          int* status, int* sync, cudaStream_t s);
+                          int* status, int* sync, cudaStream_t s, int order = 0);
 size_t ffn_sync_ints(const Problem& p);
 
 }  // namespace moe

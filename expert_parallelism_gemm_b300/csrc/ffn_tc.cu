@@ -138,6 +138,7 @@ struct FfnArgs {
     // loads have all been issued (the progress window).  Zero at launch; the
     // last CTA to leave zeroes it again.
     int* sync;
+    int order;  // FfnOrder bits
 };
 
 // ---------------------------------------------------------------- PTX ----
@@ -406,8 +407,9 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
             asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
         }
     }
-    // global memory only from here on (earlier kernels on the stream are done)
-    dep_wait();
+    // global memory only from here on (earlier kernels on the stream are done,
+    // or, with kFfnWaitAtEnd, write and read nothing this launch touches)
+    if (!(args.order & kFfnWaitAtEnd)) dep_wait();
     if (warp == 0) {
         // expert offsets; they must be non-decreasing within [0, rows_max],
         // otherwise the kernel records kDevBadIndex and computes nothing
@@ -574,6 +576,9 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
             if (!ok) break;
             if (leader) atomicAdd(progress, 1);
         }
+        // this CTA starts no further tile: the next kernel may take the SMs
+        // that the CTAs which are done leave (the first trigger of a CTA counts)
+        if (args.order & kFfnReleaseNext) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // copies still in flight must land before the CTA leaves: the leader
         // sees them on its full barriers; the other CTA once the leader's MMA
         // has released the stage they filled
@@ -738,6 +743,8 @@ tc_ffn_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ 
                          "r"(TMEM_COLS)
                          : "memory");
     }
+    // not done before the kernel this launch did not wait for at its start
+    if (args.order & kFfnWaitAtEnd) dep_wait();
     // the last CTA out zeroes the release counters for the next launch
     if (threadIdx.x == 0) {
         __threadfence();
@@ -899,7 +906,7 @@ size_t ffn_sync_ints(const Problem& p) {
 
 cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* expert_offsets,
                           const void* W1, const void* W3, const void* W2, void* h, void* yd,
-                          int* status, int* sync, cudaStream_t s) {
+                          int* status, int* sync, cudaStream_t s, int order) {
     if (p.rows_max == 0) return cudaSuccess;
     EncodeTiledFn enc = get_encoder();
     if (!enc) return cudaErrorNotSupported;
@@ -923,6 +930,7 @@ cudaError_t launch_ffn_tc(const Problem& p, const void* xd, const int32_t* exper
     a.yd = (__nv_bfloat16*)yd;
     a.status = status;
     a.sync = sync;
+    a.order = order;
     // Down tiles are several times longer than gate/up tiles (K = ffn vs d), so
     // they all go after the last gate/up tile: every cluster then ends on one
     // or two of them instead of a few clusters finishing the last expert's.

@@ -276,7 +276,10 @@ int moe_combine_shared(const moe_problem* p, const void* yd, const int32_t* topk
  * Ws1, Ws3, Ws2 as in moe_shared_expert_ffn): the routed layer, the shared
  * expert over every token, and moe_combine_shared.  With p->ffn_shared == 0
  * it is moe_layer_forward and the shared weights are ignored.
- * moe_layer_forward itself rejects p->ffn_shared != 0. */
+ * moe_layer_forward itself rejects p->ffn_shared != 0.  In the bf16 SwiGLU
+ * form the shared expert's FFN launch starts on the SMs that the routed FFN's
+ * CTAs leave as they finish (it reads only x and its own weights), and the
+ * combine starts only after both have completed. */
 int moe_layer_forward_shared(const moe_problem* p, const void* x, const void* Wg, const float* bias,
                              const void* W1, const void* W3, const void* W2, const void* Ws1,
                              const void* Ws3, const void* Ws2, const void* residual, void* y,
