@@ -51,7 +51,7 @@ METRIC = "MoE layer forward tokens/sec on 1 B300; % of HBM BW / BF16 tensor peak
 # measured them on the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum of one launch); a workload without a capture of the
 # current kernel has no entry and reports null
-FFN_DRAM_BYTES = {"mixtral_8x7b": 15990430720 + 2412177920}
+FFN_DRAM_BYTES = {"mixtral_8x7b": 16541366272 + 2411979520}
 # a launch at least this long runs under the board's power limit: its
 # roofline takes the sustained bf16 peak, shorter ones the burst peak
 SUSTAINED_MS = 2.0
