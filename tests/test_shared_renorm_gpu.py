@@ -139,6 +139,41 @@ def test_layer_forward_shared(case):
                            y2.view(torch.int32 if y2.dtype == torch.float32 else torch.int16))
 
 
+def _bits(t):
+    return t.view(torch.int32 if t.dtype == torch.float32 else torch.int16)
+
+
+def test_layer_forward_shared_matches_its_calls(case):
+    """moe_layer_forward_shared lets its shared-expert FFN start on the SMs the
+    routed FFN's CTAs leave and wait for the routed launch at its end; its
+    output equals, bit for bit, that of the same steps as separate calls with
+    a synchronisation after each, and stays so over back-to-back layers on
+    one workspace with no synchronisation between them."""
+    wl, dev, cpu, o = case
+    if not wl.ffn_shared:
+        pytest.skip("no shared expert")
+    inp = dev.inp
+    resid = torch.randn(wl.T, wl.d, generator=torch.Generator().manual_seed(6)).to(dev.dtype).cuda()
+    idx, gate, _ = dev.route(want_probs=False)
+    a = dev.assign(idx)
+    xd = dev.dispatch(a["row_token"], a["expert_offsets"])
+    yd = dev.expert_ffn(xd, a["expert_offsets"])
+    ys = torch.empty(wl.T, wl.d, dtype=dev.dtype, device="cuda")
+    moe.moe_shared_expert_ffn(dev.p, inp.x, *_shared_args(inp), ys, dev.ws, dev.ws_bytes)
+    torch.cuda.synchronize()
+    want = torch.empty(wl.T, wl.d, dtype=dev.dtype, device="cuda")
+    moe.moe_combine_shared(dev.p, yd, idx, a["slot_pos"], a["expert_offsets"], gate, ys, resid, want)
+    torch.cuda.synchronize()
+    ys_layer = [torch.empty(wl.T, wl.d, dtype=dev.dtype, device="cuda") for _ in range(3)]
+    for y in ys_layer:
+        moe.moe_layer_forward_shared(dev.p, inp.x, inp.Wg, inp.bias, inp.W1, inp.W3, inp.W2,
+                                     *_shared_args(inp), resid, y, dev.ws, dev.ws_bytes)
+    torch.cuda.synchronize()
+    assert dev.status() == moe.MOE_OK
+    for i, y in enumerate(ys_layer):
+        assert torch.equal(_bits(y), _bits(want)), f"layer {i} differs from the separate calls"
+
+
 def test_plain_entry_points_reject_a_shared_expert():
     wl = CASES["shared_odd_bf16"]
     p = moe.problem_of(wl)
