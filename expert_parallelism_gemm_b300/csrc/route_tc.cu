@@ -815,9 +815,10 @@ int sm_count() {
 
 // Up to 16 experts the fixed-order SIMT router is faster (its E multiply-adds
 // per loaded element cost less than this kernel's Gram products and per-tile
-// epilogue; measured at 8 experts: 17 against 28 us at T = 4096, 140 against
-// 162 us at T = 32768, d = 4096); above 128 the per-token logit table no
-// longer fits next to the stage ring.
+// epilogue; measured at 8 experts, one call at full clock, L2 flushed, with
+// identical indices: 11.5 against 26.7 us at T = 4096, d = 1024, and 86
+// against 115 us at T = 32768, d = 4096); above 128 the per-token logit table
+// no longer fits next to the stage ring.
 bool route_tc_eligible(const Problem& p) { return p.dtype == MOE_BF16 && p.T > 0 && p.E > 16 && p.E <= 128; }
 
 cudaError_t launch_route_tc(const Problem& p, const void* x, const void* Wg, const float* bias, int32_t* topk_idx,
