@@ -169,16 +169,17 @@ __device__ __forceinline__ void write_gates(float* gate, const float (&chosen)[8
 }
 
 // ring stages: 4 for bf16 (3 for fp32, whose chunks are twice the bytes);
-// 5 for bf16 at up to 8 experts, where the logit table is small enough that
-// the fifth stage still leaves two CTAs per SM and puts a 1024-wide hidden
-// dimension's four chunks in flight at once
+// 3 for bf16 at up to 8 experts, where 62 KB of shared memory and 80
+// registers a thread leave room for three CTAs per SM (five stages, the
+// earlier choice, left two): the 8x7B-shape router 86 -> 80 us, the one at
+// T = 4096 unchanged
 template <typename T>
 __host__ __device__ constexpr int route_stages() {
     return sizeof(T) == 2 ? 4 : 3;
 }
 template <typename T>
 constexpr int route_stages_small_e() {
-    return sizeof(T) == 2 ? 5 : 3;
+    return 3;
 }
 
 // experts per pass: 8, or 16 above 8 experts
