@@ -223,12 +223,17 @@ def run_ours(args, rank, world, local_rank):
     dropped = torch.empty(1, dtype=i32, device=dev)
     xd = torch.empty(max(rows_max, 1), wl.d, dtype=inp.x.dtype, device=dev)
     yd = torch.empty(max(rows_max, 1), wl.d, dtype=inp.x.dtype, device=dev)
+    by_token = wl.k >= 2 and wl.T * wl.d * inp.x.element_size() > l2 // 2
     calls = ["route", "assign", "dispatch", "expert_ffn", "combine"]
     call_fns = [
         lambda: moe.moe_route(p, inp.x, inp.Wg, inp.bias, idx, gate, None, ws, wsb, None),
         lambda: moe.moe_assign_slots(p, idx, slot, cr, ck, off, so, sr, sov, row_token, dropped, ws, wsb,
                                      None),
-        lambda: moe.moe_dispatch(p, inp.x, row_token, off, xd, None),
+        # the form moe_layer_forward uses: token-major for k >= 2 when x is
+        # larger than half the L2 (each x row read once for all its slots),
+        # expert-major otherwise
+        (lambda: moe.moe_dispatch_by_token(p, inp.x, idx, slot, off, xd, None)) if by_token else
+        (lambda: moe.moe_dispatch(p, inp.x, row_token, off, xd, None)),
         lambda: moe.moe_expert_ffn(p, xd, off, inp.W1, inp.W3, inp.W2, yd, ws, wsb, None),
         lambda: moe.moe_combine(p, yd, idx, slot, off, gate, None, y, None),
     ]
@@ -465,7 +470,8 @@ def run_ours(args, rank, world, local_rank):
                       "frac_hbm": gb(route_bytes, per_call["route"]) / hbm_gbs},
             "assign": {"ms": per_call["assign"]},
             "dispatch": {"ms": per_call["dispatch"], "GB_s": gb(dispatch_bytes, per_call["dispatch"]),
-                         "frac_hbm": gb(dispatch_bytes, per_call["dispatch"]) / hbm_gbs},
+                         "frac_hbm": gb(dispatch_bytes, per_call["dispatch"]) / hbm_gbs,
+                         "form": "moe_dispatch_by_token" if by_token else "moe_dispatch"},
             "expert_ffn": {"ms": per_call["expert_ffn"], "TFLOP_s": achieved_tf,
                            "frac_bf16": achieved_tf / bf16_tf,
                            "weight_GB_s": gb(weight_bytes, per_call["expert_ffn"]),

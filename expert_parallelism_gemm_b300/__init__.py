@@ -28,7 +28,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE = 4, 5, 6
 
 EXPORTS = ("moe_capacity", "moe_workspace_size", "moe_workspace_layout_of", "moe_route",
-           "moe_assign_slots", "moe_dispatch", "moe_expert_ffn", "moe_combine",
+           "moe_assign_slots", "moe_dispatch", "moe_dispatch_by_token", "moe_expert_ffn", "moe_combine",
            "moe_layer_forward", "moe_device_status", "moe_status_string",
            "moe_assign_slots_static", "moe_routing_stats", "moe_shared_expert_ffn",
            "moe_combine_shared", "moe_layer_forward_shared", "moe_expert_choice_assign",
@@ -81,6 +81,7 @@ def load() -> ctypes.CDLL:
     lib.moe_route.argtypes = [PP, P, P, P, P, P, P, P, sz, P]
     lib.moe_assign_slots.argtypes = [PP] + [P] * 11 + [sz, P]
     lib.moe_dispatch.argtypes = [PP, P, P, P, P, P]
+    lib.moe_dispatch_by_token.argtypes = [PP, P, P, P, P, P, P]
     lib.moe_expert_ffn.argtypes = [PP, P, P, P, P, P, P, P, sz, P]
     lib.moe_combine.argtypes = [PP, P, P, P, P, P, P, P, P]
     lib.moe_layer_forward.argtypes = [PP, P, P, P, P, P, P, P, P, P, sz, P]
@@ -238,6 +239,11 @@ def moe_assign_slots_static_status(stream=None) -> int:
 def moe_dispatch(problem, x, row_token, expert_offsets, xd, stream=None):
     _check(load().moe_dispatch(ctypes.byref(problem), _p(x), _p(row_token), _p(expert_offsets),
                                _p(xd), _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_by_token(problem, x, topk_idx, slot_pos, expert_offsets, xd, stream=None):
+    _check(load().moe_dispatch_by_token(ctypes.byref(problem), _p(x), _p(topk_idx), _p(slot_pos),
+                                        _p(expert_offsets), _p(xd), _stream(stream)), "moe_dispatch_by_token")
 
 
 def moe_expert_ffn(problem, xd, expert_offsets, W1, W3, W2, yd, ws, ws_bytes, stream=None):

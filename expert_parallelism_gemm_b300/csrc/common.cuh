@@ -197,6 +197,10 @@ cudaError_t launch_rank(const Problem& p, const int32_t* topk_idx, const int32_t
 
 cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_token,
                             const int32_t* expert_offsets, void* xd, cudaStream_t s);
+// the same permutation token-major: each token's x row read once, stored to
+// each of its kept slots (expert_offsets[e] + slot_pos)
+cudaError_t launch_scatter(const Problem& p, const void* x, const int32_t* topk_idx, const int32_t* slot_pos,
+                           const int32_t* expert_offsets, void* xd, cudaStream_t s);
 
 // shared: optional shared-expert output [T, d], added after the routed sum
 cudaError_t launch_combine(const Problem& p, const void* yd, const int32_t* topk_idx,

@@ -56,6 +56,55 @@ dispatch_kernel(int64_t Tn, int64_t rows_max, int E, int d, const T* __restrict_
     }
 }
 
+// Token-major form of the same permutation: one warp per token reads its x
+// row once and stores it to each of its kept slots, row expert_offsets[e] +
+// slot_pos[t, r] (the row the gather form finds through row_token).  With k
+// ranks a token's row is needed k times; the gather form reads it once per
+// slot, and those reads lie a whole expert segment apart, too far for L2 on
+// the large layers (the Mixtral 8x7B shape moved 1.07 GB for 805 MB of
+// algorithmic bytes).  Lanes r < k fetch rank r's destination; an invalid
+// expert, a dropped rank (slot -1) or a row past rows_max stores nothing.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+scatter_kernel(int64_t Tn, int64_t rows_max, int E, int d, int k, const T* __restrict__ x,
+               const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ slot_pos,
+               const int32_t* __restrict__ expert_offsets, T* __restrict__ xd) {
+    dep_wait();
+    constexpr int VE = vec_elems<T>();
+    constexpr int B = 4;  // 16-byte loads in flight per lane before the stores
+    const int nv = d / VE;
+    const int lane = threadIdx.x & 31;
+    for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < Tn;
+         t += (int64_t)gridDim.x * kWarps) {
+        int64_t row = -1;
+        if (lane < k) {
+            const int e = topk_idx[t * k + lane];
+            const int pos = slot_pos[t * k + lane];
+            if (e >= 0 && e < E && pos >= 0) {
+                const int64_t r = (int64_t)expert_offsets[e] + pos;
+                if (r < rows_max) row = r;
+            }
+        }
+        const unsigned kept = __ballot_sync(0xffffffffu, row >= 0);
+        if (!kept) continue;
+        const T* src = x + (size_t)t * d;
+        for (int v0 = lane; v0 < nv; v0 += 32 * B) {
+            Vec16 q[B];
+#pragma unroll
+            for (int j = 0; j < B; ++j)
+                if (v0 + 32 * j < nv) q[j] = ld_nc_v16(src + (v0 + 32 * j) * VE);
+            for (unsigned m = kept; m; m &= m - 1) {
+                const int r = __ffs(m) - 1;
+                const int64_t dst_row = __shfl_sync(0xffffffffu, row, r);
+                T* dst = xd + (size_t)dst_row * d;
+#pragma unroll
+                for (int j = 0; j < B; ++j)
+                    if (v0 + 32 * j < nv) st_v16(dst + (v0 + 32 * j) * VE, q[j]);
+            }
+        }
+    }
+}
+
 // CB vector columns per lane per step, each gathering up to KM ranks, so all
 // of a step's loads are issued before the first multiply-add.  CB * KM is
 // kept at 4 or 8 vectors: more would hold the kernel to two CTAs per SM by
@@ -153,6 +202,17 @@ cudaError_t launch_dispatch(const Problem& p, const void* x, const int32_t* row_
                         p.d, (const __nv_bfloat16*)x, row_token, expert_offsets, (__nv_bfloat16*)xd);
     return launch_k(dispatch_kernel<float>, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d,
                     (const float*)x, row_token, expert_offsets, (float*)xd);
+}
+
+cudaError_t launch_scatter(const Problem& p, const void* x, const int32_t* topk_idx, const int32_t* slot_pos,
+                           const int32_t* expert_offsets, void* xd, cudaStream_t s) {
+    if (p.rows_max == 0 || p.T == 0) return cudaSuccess;
+    const unsigned g = grid_for(p.T);
+    if (p.dtype == MOE_BF16)
+        return launch_k(scatter_kernel<__nv_bfloat16>, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d,
+                        p.k, (const __nv_bfloat16*)x, topk_idx, slot_pos, expert_offsets, (__nv_bfloat16*)xd);
+    return launch_k(scatter_kernel<float>, dim3(g), dim3(kThreads), 0, s, p.T, p.rows_max, p.E, p.d, p.k,
+                    (const float*)x, topk_idx, slot_pos, expert_offsets, (float*)xd);
 }
 
 template <typename T>

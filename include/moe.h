@@ -220,6 +220,20 @@ int moe_assign_slots(const moe_problem* p, const int32_t* topk_idx, int32_t* slo
 int moe_dispatch(const moe_problem* p, const void* x, const int32_t* row_token,
                  const int32_t* expert_offsets, void* xd, void* stream);
 
+/* The same dispatch, walked token by token: for every token t and rank r
+ * with slot_pos[t, r] >= 0 (the outputs of moe_assign_slots; topk_idx and
+ * slot_pos [T, k] int32),
+ *   xd[expert_offsets[topk_idx[t, r]] + slot_pos[t, r]] = x[t]
+ * which writes exactly the rows moe_dispatch writes, with the same bytes.
+ * Each row of x is read once for all of the token's slots, where the
+ * expert-major form reads it once per slot; moe_layer_forward uses this form
+ * for k >= 2 when x is larger than half the L2.  A rank whose expert is outside [0, E), whose slot is negative
+ * or whose row would reach rows_max stores nothing.  x and xd 16-byte
+ * aligned. */
+int moe_dispatch_by_token(const moe_problem* p, const void* x, const int32_t* topk_idx,
+                          const int32_t* slot_pos, const int32_t* expert_offsets, void* xd,
+                          void* stream);
+
 /* Expert computation (notes page, expert GEMM and formal algorithm;
  * ashishsrivastav.com phase 3): for every expert e and every packed row
  * r in [expert_offsets[e], expert_offsets[e+1]):

@@ -33,7 +33,7 @@ def _declared_functions():
 
 def test_every_declared_symbol_is_exported():
     names = _declared_functions()
-    assert len(names) == 27, names
+    assert len(names) == 28, names
     assert sorted(moe.EXPORTS) == names
     lib = moe.load()
     for n in names:
@@ -159,6 +159,12 @@ def test_bad_pointers_and_workspace_rejected_before_launch():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_combine(p, A, A, A, A, A, A + 2, A, stream=0)
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG  # misaligned residual
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch_by_token(p, A, A, None, A, A, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG  # slot_pos missing
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_dispatch_by_token(p, A, A, A, A, A + 8, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG  # misaligned xd
     # rerouting: the plain slot calls refuse the flag, the rerouting calls need it
     pr = _problem(reroute=True)
     need_r = moe.moe_workspace_size(pr)

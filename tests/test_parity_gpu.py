@@ -68,6 +68,14 @@ SMALL = {
                            seed=23, zipf_s=1.0),
     "pack_limit_plus1": Workload("pack_limit_plus1", T=8224, d=64, E=64, D=8, k=1, ffn=64,
                                  capacity_factor=1.0, seed=24, zipf_s=1.0),
+    # past the slot-and-pack limit with k >= 2 (rank pass, then a separate
+    # dispatch), with drops, a ragged last block and k = 8; the token-major
+    # dispatch is checked on them directly (the layer takes it where x is
+    # larger than half the L2, the Mixtral 8x7B shape)
+    "scatter_k2": Workload("scatter_k2", T=4200, d=64, E=64, D=8, k=2, ffn=64, capacity_factor=1.0,
+                           seed=26, zipf_s=1.0),
+    "scatter_k8": Workload("scatter_k8", T=4133, d=64, E=16, D=4, k=8, ffn=64, capacity_factor=1.0,
+                           seed=27),
 }
 FULL = {n: w for n, w in moe_inputs.WORKLOADS.items() if n != "tiny_fp32"}
 
@@ -140,6 +148,19 @@ def test_dispatch(case):
     s = o["slots"]
     kept = int(s.expert_offsets[-1])
     xd = dev.dispatch(t_dev(s.row_token if kept else np.zeros(1, np.int32)), t_dev(s.expert_offsets))
+    np.testing.assert_array_equal(raw(xd[:kept]), o["xd"])
+    assert (raw(xd[kept:]) == 0).all()  # untouched
+
+
+def test_dispatch_by_token(case):
+    """The token-major dispatch writes the same rows, the same bytes, as the
+    expert-major one, and leaves the rest of xd alone."""
+    name, wl, dev, cpu, o = case
+    s = o["slots"]
+    kept = int(s.expert_offsets[-1])
+    xd = torch.zeros((max(dev.rows_max, 1), wl.d), dtype=dev.dtype, device="cuda")
+    moe.moe_dispatch_by_token(dev.p, dev.inp.x, t_dev(o["idx"]), t_dev(s.slot_pos), t_dev(s.expert_offsets), xd)
+    torch.cuda.synchronize()
     np.testing.assert_array_equal(raw(xd[:kept]), o["xd"])
     assert (raw(xd[kept:]) == 0).all()  # untouched
 
@@ -258,7 +279,8 @@ def test_layer_forward(case):
 def test_layer_equals_step_by_step(case):
     """moe_layer_forward is the composition of the five calls, bit for bit."""
     name, wl, dev, cpu, o = case
-    if name not in ("ragged_bf16", "skew_64e_small", "tiny_fp32", "mixtral_scaled"):
+    if name not in ("ragged_bf16", "skew_64e_small", "tiny_fp32", "mixtral_scaled", "scatter_k2", "scatter_k8",
+                    "mixtral_8x7b"):
         pytest.skip("checked on a few workloads")
     y = dev.layer()
     idx, gate, _ = dev.route(want_probs=False)
