@@ -4,7 +4,9 @@
 // Dispatch: "Expert Parallelism and the All-to-All Bottleneck"
 // (ashishsrivastav.com), phase 2: rows are repacked so each row holds a token
 // destined for one expert; "Expert Parallelism" notes page
-// (narrativegoldmine.com), token dispatch tensor.  xd[row] = x[row_token[row]].
+// (narrativegoldmine.com), token dispatch tensor.  xd[row] = x[row_token[row]],
+// walked expert-major (a gather through row_token) or token-major (each
+// token's row stored to its k slots).
 //
 // Combine: same blog, phase 4 (results reassembled in token order); notes
 // page, expert combine (gate-weighted sum of a token's k outputs) and residual
