@@ -165,6 +165,38 @@ def test_dispatch_by_token(case):
     assert (raw(xd[kept:]) == 0).all()  # untouched
 
 
+def test_dispatch_by_token_skips_invalid_ranks():
+    """A rank whose expert is out of range or whose slot is negative stores
+    nothing; every other kept rank's row is written exactly."""
+    name, wl, dev, cpu, o = _build_case("ragged_bf16")
+    s = o["slots"]
+    kept = int(s.expert_offsets[-1])
+    idx = o["idx"].copy()
+    slot = s.slot_pos.copy()
+    rng = np.random.default_rng(31)
+    kept_pairs = np.argwhere(slot >= 0)
+    pick = kept_pairs[rng.choice(len(kept_pairs), size=40, replace=False)]
+    bad_e, bad_s = pick[:20], pick[20:]
+    skipped = set()
+    for t, r in bad_e:
+        skipped.add(int(s.expert_offsets[idx[t, r]] + slot[t, r]))
+        idx[t, r] = wl.E if t % 2 else -3
+    for t, r in bad_s:
+        skipped.add(int(s.expert_offsets[idx[t, r]] + slot[t, r]))
+        slot[t, r] = -1
+    sentinel = torch.full((max(dev.rows_max, 1), wl.d), 7.0, dtype=dev.dtype, device="cuda")
+    moe.moe_dispatch_by_token(dev.p, dev.inp.x, t_dev(idx), t_dev(slot), t_dev(s.expert_offsets), sentinel)
+    torch.cuda.synchronize()
+    got = raw(sentinel)
+    want = raw(torch.full((1, wl.d), 7.0, dtype=dev.dtype))[0]
+    for row in range(kept):
+        if row in skipped:
+            np.testing.assert_array_equal(got[row], want)
+        else:
+            np.testing.assert_array_equal(got[row], o["xd"][row])
+    assert (got[kept:] == want).all()
+
+
 def _oracle_xd_tensor(o, dev):
     xd = torch.zeros((max(dev.rows_max, 1), dev.wl.d), dtype=dev.dtype)
     kept = int(o["slots"].expert_offsets[-1])
