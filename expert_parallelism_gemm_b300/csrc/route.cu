@@ -169,10 +169,12 @@ __device__ __forceinline__ void write_gates(float* gate, const float (&chosen)[8
 }
 
 // ring stages: 4 for bf16 (3 for fp32, whose chunks are twice the bytes);
-// 3 for bf16 at up to 8 experts, where 62 KB of shared memory and 80
-// registers a thread leave room for three CTAs per SM (five stages, the
-// earlier choice, left two): the 8x7B-shape router 86 -> 80 us, the one at
-// T = 4096 unchanged
+// at up to 8 experts 3, where 62 KB of shared memory and 80 registers a thread
+// leave room for three CTAs per SM (five stages, the earlier choice, left
+// two), and for bf16 rows longer than 1024 elements 2, with four CTAs per SM
+// (64 registers).  Measured with identical indices: the 8x7B-shape router
+// (d = 4096) 86 us with five stages, 80 with three, 76 with two; the one at
+// T = 4096, d = 1024, 11.0 us with three or five, 12.4 with two.
 template <typename T>
 __host__ __device__ constexpr int route_stages() {
     return sizeof(T) == 2 ? 4 : 3;
@@ -181,6 +183,7 @@ template <typename T>
 constexpr int route_stages_small_e() {
     return 3;
 }
+constexpr int kRouteStagesLongRows = 2;  // bf16, up to 8 experts, d > 1024
 
 // experts per pass: 8, or 16 above 8 experts
 template <int RE>
@@ -191,7 +194,7 @@ size_t route_smem_bytes(int elem_bytes, int stages, int E, int k) {
 }
 
 template <typename T, int RE, int S>
-__global__ void __launch_bounds__(kRouteThreads, 2)
+__global__ void __launch_bounds__(kRouteThreads, S == 2 ? 4 : 2)
 route_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw, int64_t T_, int d,
              int E, int k, const float* __restrict__ bias, int32_t* __restrict__ topk_idx,
              float* __restrict__ topk_gate, float* __restrict__ probs, float* __restrict__ logits,
@@ -492,6 +495,11 @@ cudaError_t launch_route_t(const Problem& p, const void* x, const void* Wg, cons
                            int32_t* topk_idx, float* topk_gate, float* probs, float* logits,
                            int32_t* fb_idx, float* fb_gate, int* status, const AssignScan& scan,
                            cudaStream_t s) {
+    if constexpr (sizeof(T) == 2) {
+        if (p.E <= 8 && p.d > 1024)
+            return launch_route_re<T, 8, kRouteStagesLongRows>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits,
+                                                               fb_idx, fb_gate, status, scan, s);
+    }
     if (p.E <= 8)
         return launch_route_re<T, 8, route_stages_small_e<T>()>(p, x, Wg, bias, topk_idx, topk_gate, probs, logits,
                                                                 fb_idx, fb_gate, status, scan, s);

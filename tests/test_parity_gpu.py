@@ -76,6 +76,10 @@ SMALL = {
                            seed=26, zipf_s=1.0),
     "scatter_k8": Workload("scatter_k8", T=4133, d=64, E=16, D=4, k=8, ffn=64, capacity_factor=1.0,
                            seed=27),
+    # rows longer than 1024 at up to 8 experts: the router's two-stage ring
+    # (four CTAs per SM), with a ragged last 256-element chunk
+    "long_rows_bf16": Workload("long_rows_bf16", T=300, d=1096, E=8, D=4, k=2, ffn=64, capacity_factor=1.0,
+                               seed=28),
 }
 FULL = {n: w for n, w in moe_inputs.WORKLOADS.items() if n != "tiny_fp32"}
 
